@@ -1,0 +1,80 @@
+// Internal declarations shared by the host side of libkvb and its kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+#include <string>
+
+#include "../../include/kvb.h"
+#include "sm103_ptx.cuh"
+
+namespace kvb {
+
+constexpr int MAX_LT = 128;  // target layers a context can describe
+constexpr int MAX_LS = 255;  // source layers (selection entries are bytes)
+constexpr int MAX_K = 16;    // top_k
+
+// Selection table passed by value to kernels: [kv][target layer][j].
+struct SelTable {
+    uint8_t s[2][MAX_LT][MAX_K];
+};
+
+struct Shape {
+    int L_s, L_t, H, d, k;
+    int64_t T;
+    int max_pos;
+};
+
+// ------------------------------------------------------------ launchers
+// RoPE cos/sin table: tab[p][i] = (cos(p w_i), sin(p w_i)), w_i = theta^(-2i/d).
+cudaError_t launch_rope_table(float2* tab, int max_pos, int d, double theta, cudaStream_t s);
+
+// Strip source RoPE from bf16 keys [LH][T][d] into `out` (same layout).
+cudaError_t launch_strip_bf16(const __nv_bfloat16* in, __nv_bfloat16* out, const int* pos,
+                              const float2* tab, int64_t LH, int64_t T, int d, int max_pos,
+                              DevErr err, int num_sms, cudaStream_t s);
+
+// tcgen05 mapper GEMM with fused bias + target RoPE epilogue (bf16, d == 128).
+struct MapGemmArgs {
+    Shape sh;
+    const void* a_src[2];   // [L_s*H][T][d] bf16: stripped keys, raw values
+    const void* w[2];       // [L_t][q][p] bf16
+    const float* bias[2];   // [L_t][q]
+    void* out[2];           // [L_t][H][T][d] bf16
+    const int* pos;
+    const float2* tab_t;    // target RoPE table
+    SelTable sel;
+    DevErr err;
+    int num_sms;
+};
+bool map_gemm_tc_supported(const Shape& sh);
+cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string* why);
+
+// SIMT mapper (any even d with d % 8 == 0): strip fused into the operand load,
+// bias + target RoPE in the epilogue.  dtype selects fp32 or bf16 storage.
+struct MapSimtArgs {
+    Shape sh;
+    kvb_dtype dtype;
+    const void* src[2];
+    const void* w[2];
+    const float* bias[2];
+    void* out[2];
+    const int* pos;
+    const float2* tab_s;
+    const float2* tab_t;
+    SelTable sel;
+    DevErr err;
+};
+cudaError_t launch_map_simt(const MapSimtArgs& a, cudaStream_t s);
+
+// Tensor-map encoder fetched from the driver at run time.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_tiled();
+
+}  // namespace kvb

@@ -1,0 +1,203 @@
+/*
+ * kvb.h -- C ABI of libkvb, closed-form cross-model KV-cache transfer on GB300.
+ *
+ * The method (Heo et al., "Cross-Model KV Cache Transfer in LLM Families"),
+ * as the pages state it:
+ *   "Cross-Model KV Transfer -- Reuse One Model's Prefill in Another"
+ *   (VeloxQuant-MLX docs), section "The mapping":
+ *       K_hat_t = rope_t( strip_rope_s(K_s)[sel] . W_K + b_K )
+ *       V_hat_t =               V_s[sel]    . W_V + b_V
+ *   "KVBridge" README, section "Loading":
+ *       W = (X^T X + lambda I)^-1 X^T Y,  b = Ybar - Xbar W  on centered data,
+ *       batchwise Chan/Welford merges of the centered statistics;
+ *   "KVBridge" README, table "What ships": head-averaged single-source R^2,
+ *       then top-k cross-layer, cross-head features.
+ *
+ * Layouts (all row-major, innermost last):
+ *   cache      [L][H][T][d]   (layer, kv head, token, dim) -- "Before Mapping KV
+ *                             Caches, Make Them Measurable", "what became
+ *                             first-class".  Ragged batches pack sequences on T
+ *                             with positions restarting at 0 per sequence.
+ *   features   X_t[token][(j*H + h)*d + e] = cache[sel[t][j]][h][token][e]
+ *                             (selected layers in the order given, then head,
+ *                             then dim); p = k*H*d columns.
+ *   W          [L_tgt][q][p], q = H*d: row n holds the p input weights of
+ *                             output column n (a linear layer's weight layout;
+ *                             the mathematical W is its transpose).
+ *   bias       [L_tgt][q] float32.
+ *   sel        [L_tgt][k] int32 on the HOST, one table for K and one for V.
+ *   positions  [T] int32 on the DEVICE, 0 <= pos < max_pos (checked in the
+ *                             kernels; a bad position sets KVB_ERR_INVALID_ARG
+ *                             on the context and its rows are written as 0).
+ *
+ * RoPE: rotate-half pairs (i, i + d/2), frequency theta^(-2i/d); angles are
+ * reduced in float64 once per context into float32 cos/sin tables.
+ *
+ * Ownership: the caller owns every tensor passed in.  The library allocates
+ * only inside a context (RoPE tables, strip scratch, error word) and a
+ * statistics object, and frees on destroy.
+ *
+ * Streams and errors: calls enqueue work on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and return without a host sync, except
+ * kvb_layer_select, which syncs `stream` to hand back the selection.
+ * Arguments are validated on the host before any launch.  No call aborts the
+ * process: every failure is a returned status, with a message from
+ * kvb_last_error().  Errors found by the kernels themselves (a bad position,
+ * a bounded device wait that gave up) are recorded on the context and returned
+ * by kvb_ctx_check() and by the next call on that context.
+ */
+#ifndef KVB_H
+#define KVB_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVB_OK = 0,
+    KVB_ERR_INVALID_ARG = 1,    /* null pointer, bad size, bad selection, misaligned pointer */
+    KVB_ERR_SHAPE_MISMATCH = 2, /* source and target KV heads / head dims differ */
+    KVB_ERR_UNSUPPORTED = 3,    /* interleaved RoPE, rope_scaling, odd head_dim, dtype */
+    KVB_ERR_CUDA = 4,           /* a CUDA runtime or driver call failed */
+    KVB_ERR_NUMERIC = 5,        /* a system was not positive definite, or non-finite data */
+    KVB_ERR_OOM = 6,            /* device allocation failed */
+    KVB_ERR_TIMEOUT = 7         /* a bounded device wait gave up */
+} kvb_status;
+
+typedef enum { KVB_F32 = 0, KVB_BF16 = 1 } kvb_dtype;
+
+/* One model's KV geometry ("KVBridge" ModelSignature; VeloxQuant ModelKVSpec). */
+typedef struct {
+    int32_t n_layers;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    double rope_theta;
+    int32_t rope_interleaved; /* 1 = interleaved ("traditional") pairs: refused */
+    int32_t rope_scaling;     /* 1 = any rope_scaling: refused */
+} kvb_model_spec;
+
+typedef struct kvb_ctx kvb_ctx;
+typedef struct kvb_stats kvb_stats;
+
+/* Message of the last failed call on this thread ("" if none).  Never NULL. */
+const char* kvb_last_error(void);
+
+/* Library version, (major << 16) | minor. */
+int32_t kvb_version(void);
+
+/*
+ * Create a context for one (source, target) pair on CUDA device `device`.
+ * Refusals ("Cross-Model KV Transfer", "The honesty crux" item 7): mismatched
+ * KV heads or head_dim -> KVB_ERR_SHAPE_MISMATCH; interleaved RoPE or
+ * rope_scaling -> KVB_ERR_UNSUPPORTED; odd head_dim -> KVB_ERR_UNSUPPORTED.
+ * top_k in [1, src->n_layers]; max_pos >= 1 sizes the RoPE tables.
+ * Builds both cos/sin tables (float64 angle reduction) and waits for them.
+ */
+kvb_status kvb_ctx_create(const kvb_model_spec* src, const kvb_model_spec* tgt, int32_t top_k,
+                          int32_t max_pos, int32_t device, kvb_ctx** out);
+
+/* Free everything the context owns (syncs the device first).  NULL is a no-op. */
+kvb_status kvb_ctx_destroy(kvb_ctx* ctx);
+
+/* Pre-size the strip scratch for up to T tokens so kvb_map_apply never allocates. */
+kvb_status kvb_ctx_reserve(kvb_ctx* ctx, int64_t T);
+
+/* Sync `stream` and report (then clear) errors the kernels recorded on ctx. */
+kvb_status kvb_ctx_check(kvb_ctx* ctx, void* stream);
+
+/*
+ * Kernel timing for measurement.  While enabled, every kernel the context
+ * launches is bracketed by CUDA events recorded on its launch stream.
+ * kvb_profile_read waits for the recorded events, writes one entry per kernel
+ * name (launch count and summed device time since the last read) and clears
+ * the record.  `count` receives the number of entries written (<= cap).
+ */
+typedef struct {
+    char name[32];
+    int64_t launches;
+    double total_ms;
+} kvb_kernel_time;
+
+kvb_status kvb_profile_enable(kvb_ctx* ctx, int32_t on);
+kvb_status kvb_profile_read(kvb_ctx* ctx, kvb_kernel_time* out, int32_t cap, int32_t* count);
+
+/*
+ * Map a source cache into a target cache ("Cross-Model KV Transfer", "The
+ * mapping"; "KV-Cache zwischen Qwen3-Modellen ...", map_cache sketch).
+ *   dtype       KVB_BF16: bf16 caches and W, fp32 accumulation, bf16 output
+ *                         (round to nearest even); KVB_F32: fp32 throughout.
+ *   src_k/src_v device [L_src][H][T][d] (keys as stored, i.e. with source RoPE)
+ *   positions   device [T] int32
+ *   sel_k/sel_v host   [L_tgt][k] int32, entries distinct within a row, in range
+ *   W_k/W_v     device [L_tgt][H*d][k*H*d]  (dtype)
+ *   b_k/b_v     device [L_tgt][H*d] float32
+ *   out_k/out_v device [L_tgt][H][T][d] (dtype), fully overwritten
+ * T == 0 is a no-op.  Device pointers must be 16-byte aligned.
+ */
+kvb_status kvb_map_apply(kvb_ctx* ctx, kvb_dtype dtype, const void* src_k, const void* src_v,
+                         const int32_t* positions, int64_t T, const int32_t* sel_k,
+                         const int32_t* sel_v, const void* W_k, const void* W_v, const float* b_k,
+                         const float* b_v, void* out_k, void* out_v, void* stream);
+
+/*
+ * Calibration statistics ("KVBridge" README, "Loading").  One object holds, for
+ * K and for V, the observation count n, the feature and target means, the
+ * centered Gram over ALL source features (L_src*H*d square), the centered
+ * cross statistics against ALL target columns (L_src*H*d x L_tgt*H*d) and the
+ * per-column target sum of squares, all float32.  Per-target statistics for
+ * any selection are sub-blocks of these (centering commutes with choosing
+ * columns).  max_batch_tokens bounds T of one kvb_stats_accumulate call.
+ */
+kvb_status kvb_stats_create(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_batch_tokens,
+                            kvb_stats** out);
+kvb_status kvb_stats_destroy(kvb_stats* st);
+
+/* Zero the statistics (n = 0), asynchronously on `stream`. */
+kvb_status kvb_stats_reset(kvb_stats* st, void* stream);
+
+/*
+ * Fold one batch of calibration tokens into `st` with a Chan merge.
+ *   src_k/src_v device [L_src][H][T][d], tgt_k/tgt_v device [L_tgt][H][T][d]
+ *   (dtype of the statistics object; keys as stored, with RoPE), positions
+ *   device [T].  Tokens with pos % stride == 0 are kept ("Cross-Model KV
+ *   Transfer", "Configuration": stride 4).  Keys are stripped with their own
+ *   model's theta; values are used raw.
+ */
+kvb_status kvb_stats_accumulate(kvb_ctx* ctx, kvb_stats* st, const void* src_k, const void* src_v,
+                                const void* tgt_k, const void* tgt_v, const int32_t* positions,
+                                int64_t T, int32_t stride, void* stream);
+
+/* Observation count so far (syncs `stream`). */
+kvb_status kvb_stats_count(kvb_stats* st, int64_t* n_obs, void* stream);
+
+/*
+ * Head-averaged single-source R^2 and top-k ("KVBridge" README, "What ships").
+ * For each kv in {K, V}, source layer s and target layer t: the ridge fit of
+ * target t from source s alone (lambda absolute, centered), per-column
+ * SSE = S_yy - diag(C^T W) - lambda diag(W^T W), per-head pooled
+ * R^2_h = 1 - sum SSE / sum S_yy over the head's d columns, averaged over heads.
+ * Top-k per target by (R^2 descending, source index ascending), written in
+ * ascending order to sel_k_host / sel_v_host [L_tgt][k].  r2 (device, float32
+ * [2][L_tgt][L_src], K first) may be NULL.  Syncs `stream`.
+ */
+kvb_status kvb_layer_select(kvb_ctx* ctx, kvb_stats* st, double lambda, int32_t* sel_k_host,
+                            int32_t* sel_v_host, float* r2, void* stream);
+
+/*
+ * Ridge solve per target layer ("KVBridge" README, "Loading"): with the
+ * centered statistics gathered for the selection, W = (M + lambda I)^-1 C and
+ * b = ybar - xbar W.  W_k/W_v device [L_tgt][H*d][k*H*d] in w_dtype (float32
+ * solve, rounded once on output for KVB_BF16), b_k/b_v device [L_tgt][H*d]
+ * float32.  Returns KVB_ERR_NUMERIC if a system is not positive definite.
+ */
+kvb_status kvb_ridge_solve(kvb_ctx* ctx, kvb_stats* st, const int32_t* sel_k_host,
+                           const int32_t* sel_v_host, double lambda, kvb_dtype w_dtype, void* W_k,
+                           void* W_v, float* b_k, float* b_v, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVB_H */

@@ -1,0 +1,160 @@
+"""GPU parity of kvb_map_apply against the float64 oracle, through the C ABI.
+
+Small cases compare every element; the full-size pair shapes compare sampled
+target layers x sampled tokens (rows and layers are independent, so the
+oracle on a slice is exact for that slice)."""
+import numpy as np
+import pytest
+
+from cases import TOL_BF16, TOL_F32, ApplyCase, rel_fro, spec
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvb():
+    from cross_model_kv_gb300 import build
+    build.build()
+    import cross_model_kv_gb300 as m
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return m
+
+
+def _ctx(kvb, c, max_pos):
+    return kvb.kvb_ctx_create(spec(c.L_s, c.H, c.d, c.theta_s), spec(c.L_t, c.H, c.d, c.theta_t), c.k, max_pos)
+
+
+def _check_all(kvb, c, max_pos, tol, layers=None, tokens=None):
+    ctx = _ctx(kvb, c, max_pos)
+    c.run(kvb, ctx)
+    kvb.kvb_ctx_check(ctx)
+    ok, ov = c.oracle(layers, tokens)
+    gk, gv = c.gpu(layers, tokens)
+    ek, ev = rel_fro(gk, ok), rel_fro(gv, ov)
+    assert ek <= tol and ev <= tol, (ek, ev)
+    return ek, ev
+
+
+def test_tiny_pair_fp32(kvb):
+    # tiny synthetic pair: 4 -> 6 layers, 2 KV heads, head_dim 16, k = 2, theta 1e4 -> 5e4
+    c = ApplyCase(4, 6, 2, 16, 2, 256, 1e4, 5e4, torch.float32, seed=11, sigma=0.5)
+    ek, ev = _check_all(kvb, c, 256, TOL_F32)
+    assert ek < 1e-5 and ev < 1e-5
+
+
+def test_tiny_pair_fp32_ragged_positions(kvb):
+    from synth import packed_positions, ragged_lengths
+    pos = packed_positions(ragged_lengths(3, 5, 1, 120))
+    c = ApplyCase(4, 6, 2, 16, 2, len(pos), 1e4, 5e4, torch.float32, seed=12, positions=pos, sigma=0.5)
+    _check_all(kvb, c, 128, TOL_F32)
+
+
+def test_bf16_tensor_core_ragged_tail(kvb):
+    # 2 heads x 128 = one 256-wide N tile, T = 300 (two full M tiles and a ragged one)
+    c = ApplyCase(3, 2, 2, 128, 2, 300, 1e6, 1e6, torch.bfloat16, seed=21)
+    _check_all(kvb, c, 512, TOL_BF16)
+
+
+def test_bf16_tensor_core_several_n_tiles_random_positions(kvb):
+    rng = np.random.default_rng(5)
+    pos = rng.integers(0, 32768, size=1000).astype(np.int32)
+    c = ApplyCase(5, 3, 8, 128, 3, 1000, 1e4, 5e5, torch.bfloat16, seed=22, positions=pos)
+    _check_all(kvb, c, 32768, TOL_BF16)
+
+
+def test_bf16_tensor_core_single_token(kvb):
+    c = ApplyCase(2, 2, 2, 128, 1, 1, 1e4, 1e6, torch.bfloat16, seed=23, positions=[7])
+    _check_all(kvb, c, 8, TOL_BF16)
+
+
+def test_bf16_cuda_core_path_head_dim_64(kvb):
+    c = ApplyCase(3, 2, 4, 64, 2, 200, 1e4, 1e6, torch.bfloat16, seed=24)
+    _check_all(kvb, c, 256, TOL_BF16)
+
+
+def test_fp32_head_dim_128(kvb):
+    c = ApplyCase(3, 2, 2, 128, 2, 130, 1e6, 5e5, torch.float32, seed=25, positions=np.arange(130) * 200)
+    _check_all(kvb, c, 32768, TOL_F32)
+
+
+def test_empty_input_is_a_no_op(kvb):
+    c = ApplyCase(2, 2, 2, 128, 1, 0, 1e4, 1e4, torch.bfloat16, seed=26)
+    ctx = _ctx(kvb, c, 8)
+    c.run(kvb, ctx)
+    kvb.kvb_ctx_check(ctx)
+
+
+def test_deterministic_bits(kvb):
+    c = ApplyCase(4, 2, 8, 128, 2, 777, 1e6, 1e6, torch.bfloat16, seed=27)
+    ctx = _ctx(kvb, c, 1024)
+    c.run(kvb, ctx)
+    a = (c.out_k.clone(), c.out_v.clone())
+    c.out_k.zero_()
+    c.out_v.zero_()
+    c.run(kvb, ctx)
+    assert torch.equal(a[0], c.out_k) and torch.equal(a[1], c.out_v)
+
+
+def test_bad_position_is_reported_and_row_zeroed(kvb):
+    pos = np.arange(256, dtype=np.int32)
+    pos[17] = 5000  # beyond max_pos = 256
+    c = ApplyCase(2, 2, 2, 128, 1, 256, 1e4, 1e6, torch.bfloat16, seed=28, positions=pos)
+    ctx = _ctx(kvb, c, 256)
+    c.run(kvb, ctx)
+    with pytest.raises(kvb.KvbError) as e:
+        kvb.kvb_ctx_check(ctx)
+    assert e.value.status == 1
+    assert torch.count_nonzero(c.out_k[:, :, 17]).item() == 0
+    kvb.kvb_ctx_check(ctx)  # cleared once reported
+
+
+def test_invalid_selection_rejected_before_launch(kvb):
+    c = ApplyCase(3, 2, 2, 128, 2, 64, 1e4, 1e4, torch.bfloat16, seed=29)
+    ctx = _ctx(kvb, c, 64)
+    bad = c.sel_k.copy()
+    bad[0] = [1, 1]
+    with pytest.raises(kvb.KvbError):
+        kvb.kvb_map_apply(ctx, c.src_k, c.src_v, c.positions, bad, c.sel_v, c.W_k, c.W_v, c.b_k, c.b_v,
+                          c.out_k, c.out_v)
+    bad[0] = [0, 3]
+    with pytest.raises(kvb.KvbError):
+        kvb.kvb_map_apply(ctx, c.src_k, c.src_v, c.positions, bad, c.sel_v, c.W_k, c.W_v, c.b_k, c.b_v,
+                          c.out_k, c.out_v)
+
+
+def _sampled_tokens(T, n, seed):
+    rng = np.random.default_rng(seed)
+    idx = np.unique(np.concatenate([rng.choice(T, size=n, replace=False), [0, T - 1]]))
+    return idx
+
+
+def test_qwen3_0p6b_to_1p7b_shape_T4096(kvb):
+    # 28 -> 28 layers, 8 KV heads, head_dim 128, theta 1e6 both, k = 4, T = 4096
+    c = ApplyCase(28, 28, 8, 128, 4, 4096, 1e6, 1e6, torch.bfloat16, seed=31, host=False)
+    _check_all(kvb, c, 4096, TOL_BF16, layers=[0, 13, 27], tokens=_sampled_tokens(4096, 512, 1))
+    del c
+    torch.cuda.empty_cache()
+
+
+def test_qwen3_14b_to_32b_shape_T32768(kvb):
+    # 40 -> 64 layers, 8 KV heads, head_dim 128, theta 1e6, k = 8, T = 32768
+    c = ApplyCase(40, 64, 8, 128, 8, 32768, 1e6, 1e6, torch.bfloat16, seed=32, host=False)
+    _check_all(kvb, c, 32768, TOL_BF16, layers=[0, 31, 63], tokens=_sampled_tokens(32768, 384, 2))
+    del c
+    torch.cuda.empty_cache()
+
+
+def test_llama_8b_to_70b_shape_ragged_batch(kvb):
+    # 32 -> 80 layers, 8 KV heads, head_dim 128, theta 5e5, k = 8; 16 sequences with
+    # lengths uniform in [2048, 32768] packed on the token axis, positions restart.
+    from synth import packed_positions, ragged_lengths
+    lens = ragged_lengths(7, 16, 2048, 32768)
+    pos = packed_positions(lens)
+    c = ApplyCase(32, 80, 8, 128, 8, len(pos), 5e5, 5e5, torch.bfloat16, seed=33, positions=pos, host=False)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    tok = np.unique(np.concatenate([_sampled_tokens(len(pos), 256, 3), starts, starts + lens - 1]))
+    _check_all(kvb, c, 32768, TOL_BF16, layers=[0, 79], tokens=tok)
+    del c
+    torch.cuda.empty_cache()

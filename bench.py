@@ -1,0 +1,380 @@
+#!/usr/bin/env python
+"""Throughput of the mapper apply (kvb_map_apply) on a Qwen3-14B->32B-shaped pair.
+
+Workload: synthetic bf16 caches shaped like Qwen3-14B -> Qwen3-32B (40 -> 64
+layers, 8 KV heads, head_dim 128, RoPE theta 1e6 both), k = 8 selected source
+layers per target layer, one sequence of T = 32768 tokens at positions 0..T-1.
+One step = one kvb_map_apply call (RoPE strip pass + tcgen05 map GEMM with the
+fused bias / target-RoPE epilogue) on inputs resident in HBM.  Inputs plus
+outputs (~16 GB per step) are far larger than the 129 MB L2, so no flush is
+needed between steps.
+
+Prints ONE JSON line (rank 0).  --impl reference times the float64 oracle on
+the host cores instead (bounded samples of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "mapped tokens/s, 14B→32B shape k=8 T=32768 (ms/map, % bf16 TC peak)"
+W = dict(L_s=40, L_t=64, H=8, d=128, k=8, T=32768, theta_s=1e6, theta_t=1e6, sigma=1.0)
+P_FEAT = W["k"] * W["H"] * W["d"]          # 8192 features per target layer
+Q_OUT = W["H"] * W["d"]                    # 1024 outputs per target layer
+FLOP_PER_TOKEN = 2 * 2 * W["L_t"] * P_FEAT * Q_OUT   # K and V, 2 flop per MAC
+PAGES_MS_AT_32K = 277.6                   # pages' mapper latency, 14B->32B at 32,768 tokens (8xH100 node)
+GEMM_KERNEL = "map_gemm_tcgen05"
+STRIP_KERNEL = "rope_strip_bf16"
+
+
+def config_dict():
+    return {"workload": "qwen3-14b->32b-shaped kvb_map_apply, bf16, single sequence",
+            "L_src": W["L_s"], "L_tgt": W["L_t"], "n_kv_heads": W["H"], "head_dim": W["d"], "top_k": W["k"],
+            "T": W["T"], "rope_theta_src": W["theta_s"], "rope_theta_tgt": W["theta_t"],
+            "l2": "inputs larger than L2 (~16 GB read+written per step vs 129 MB L2), no flush",
+            "parallelism": "replicas (one independent map per GPU)"}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
+    src = os.path.join(ROOT, "cross_model_kv_gb300", "csrc", "map_gemm_sm103.cu" if kernel == GEMM_KERNEL else "rope.cu")
+    try:
+        vals = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if vals.get("source_sha256_16") != sha:
+            return None
+        return float(vals["dram_bytes_per_launch_full_workload"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "power_w_max": float(max(power)),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+
+def oracle_rate(src_k, src_v, pos, sel_k, sel_v, Wk, bk, Wv, bv, layers):
+    """Time the float64 oracle on host arrays for the given target layers; mapped tokens/s."""
+    import oracle as O
+    T = src_k.shape[2]
+    t0 = time.perf_counter()
+    O.map_apply(src_k, src_v, pos, sel_k[layers], sel_v[layers], Wk, bk, Wv, bv, W["theta_s"], W["theta_t"],
+                W["H"], W["d"])
+    dt = time.perf_counter() - t0
+    return T * (len(layers) / W["L_t"]) / dt, dt
+
+
+def host_sample(T: int, n_layers: int, seed: int):
+    """Host copy of a bounded sample of the workload: T tokens, the first n_layers target layers."""
+    import synth
+    sel_k = synth.hidden_selection(seed + 1, W["L_s"], W["L_t"], W["k"])
+    sel_v = synth.hidden_selection(seed + 2, W["L_s"], W["L_t"], W["k"])
+    sk = synth.content(seed + 3, W["L_s"], W["H"], T, W["d"], W["sigma"])
+    sv = synth.content(seed + 4, W["L_s"], W["H"], T, W["d"], W["sigma"])
+    Wk, bk = synth.hidden_weights(seed + 5, n_layers, P_FEAT, Q_OUT)
+    Wv, bv = synth.hidden_weights(seed + 6, n_layers, P_FEAT, Q_OUT)
+    return sk, sv, np.arange(T), sel_k, sel_v, Wk, bk, Wv, bv
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    T_s, n_l = 2048, 2
+    data = host_sample(T_s, n_l, seed=1)
+    layers = np.arange(n_l)
+    for _ in range(args.warmup):
+        oracle_rate(*data, layers)
+    rates, secs = [], 0.0
+    for _ in range(args.steps):
+        r, dt = oracle_rate(*data, layers)
+        rates.append(r)
+        secs += dt
+    value = float(np.mean(rates))
+    sample = f"{n_l} of {W['L_t']} target layers x {T_s} tokens per step, float64, scaled to a full map"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * W["T"] / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_dict(),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import synth
+
+    from cross_model_kv_gb300 import build as kbuild
+    kbuild.build()
+    import cross_model_kv_gb300 as kvb
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    seed = 1
+    L_s, L_t, H, d, k, T = W["L_s"], W["L_t"], W["H"], W["d"], W["k"], W["T"]
+    sel_k = synth.hidden_selection(seed + 1, L_s, L_t, k)
+    sel_v = synth.hidden_selection(seed + 2, L_s, L_t, k)
+    src_k = synth.torch_content(seed + 3, L_s, H, T, d, W["sigma"], torch.bfloat16, dev)
+    src_v = synth.torch_content(seed + 4, L_s, H, T, d, W["sigma"], torch.bfloat16, dev)
+    W_k, b_k = synth.torch_weights(seed + 5, L_t, P_FEAT, Q_OUT, torch.bfloat16, dev)
+    W_v, b_v = synth.torch_weights(seed + 6, L_t, P_FEAT, Q_OUT, torch.bfloat16, dev)
+    pos = torch.arange(T, dtype=torch.int32, device=dev)
+    out_k = torch.empty((L_t, H, T, d), dtype=torch.bfloat16, device=dev)
+    out_v = torch.empty_like(out_k)
+    spec = lambda L, th: {"n_layers": L, "n_kv_heads": H, "head_dim": d, "rope_theta": th}
+    ctx = kvb.kvb_ctx_create(spec(L_s, W["theta_s"]), spec(L_t, W["theta_t"]), k, T, local_rank)
+    kvb.kvb_ctx_reserve(ctx, T)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kvb.kvb_map_apply(ctx, src_k, src_v, pos, sel_k, sel_v, W_k, W_v, b_k, b_v, out_k, out_v, stream)
+
+    for _ in range(args.warmup):
+        step()
+    kvb.kvb_ctx_check(ctx, stream)
+
+    # ---------------- timed region (device-resident inputs)
+    clocks = ClockSampler(local_rank)
+    kvb.kvb_profile_read(ctx)
+    kvb.kvb_profile_enable(ctx, True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)  # first sample lands inside the timed region
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    kvb.kvb_profile_enable(ctx, False)
+    kernels = kvb.kvb_profile_read(ctx)
+    kvb.kvb_ctx_check(ctx, stream)
+    total_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1000.0)
+    launches = sum(n for n, _ in kernels.values())
+
+    if args.skip_extras:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s", "ms_per_step": ms_per_step,
+                              "workload": args.workload, "kernels": kernels}), flush=True)
+        return
+
+    # ---------------- end to end: pinned host buffers, copies inside the timed region
+    h_src_k = torch.empty(src_k.shape, dtype=src_k.dtype, pin_memory=True)
+    h_src_v = torch.empty(src_v.shape, dtype=src_v.dtype, pin_memory=True)
+    h_pos = torch.empty(pos.shape, dtype=pos.dtype, pin_memory=True)
+    h_out_k = torch.empty(out_k.shape, dtype=out_k.dtype, pin_memory=True)
+    h_out_v = torch.empty(out_v.shape, dtype=out_v.dtype, pin_memory=True)
+    h_src_k.copy_(src_k)
+    h_src_v.copy_(src_v)
+    h_pos.copy_(pos)
+    h2d = h_src_k.numel() * 2 + h_src_v.numel() * 2 + h_pos.numel() * 4
+    d2h = h_out_k.numel() * 2 + h_out_v.numel() * 2
+
+    def e2e_step():
+        src_k.copy_(h_src_k, non_blocking=True)
+        src_v.copy_(h_src_v, non_blocking=True)
+        pos.copy_(h_pos, non_blocking=True)
+        step()
+        h_out_k.copy_(out_k, non_blocking=True)
+        h_out_v.copy_(out_v, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_step()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * T * e2e_steps / (e2e_ms / 1000.0)
+    kvb.kvb_ctx_check(ctx, stream)
+    del h_src_k, h_src_v, h_out_k, h_out_v
+
+    if rank != 0:
+        return
+
+    peaks, peak_kind = measured_peaks()
+    gemm_n, gemm_ms = kernels.get(GEMM_KERNEL, (0, 0.0))
+    strip_n, strip_ms = kernels.get(STRIP_KERNEL, (0, 0.0))
+    gemm_avg = gemm_ms / max(gemm_n, 1)
+    strip_avg = strip_ms / max(strip_n, 1)
+    flop = FLOP_PER_TOKEN * T
+    achieved = flop / (gemm_avg / 1000.0) / 1e12
+    peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    strip_bytes = 2 * (L_s * H * T * d * 2)
+    strip_gbs = strip_bytes / (strip_avg / 1000.0) / 1e9 if strip_avg > 0 else None
+
+    # ---------------- CPU baseline: the oracle, bounded sample of the same workload (rank 0 only)
+    tok = torch.arange(0, 4096, dtype=torch.int64, device=dev)
+    n_l = 4
+    li = torch.arange(n_l, device=dev)
+    hs = lambda x: x.to(dtype=torch.float64).cpu().numpy()
+    sample = (hs(src_k.index_select(2, tok)), hs(src_v.index_select(2, tok)), np.arange(4096), sel_k, sel_v,
+              np.transpose(hs(W_k.index_select(0, li)), (0, 2, 1)), hs(b_k.index_select(0, li)),
+              np.transpose(hs(W_v.index_select(0, li)), (0, 2, 1)), hs(b_v.index_select(0, li)))
+    cpu_rate, cpu_s = oracle_rate(*sample, np.arange(n_l))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / (T / (PAGES_MS_AT_32K / 1000.0)),
+        "vs_baseline_note": "pages' 277.6 ms per 32,768-token map on an 8xH100 node (context, other hardware)",
+        "dtype": "bf16", "data": "synthetic", "config": config_dict(),
+        "tflops_effective": flop / (ms_per_step / 1000.0) / 1e12,
+        "roofline": {"bound": "tensor", "kernel": GEMM_KERNEL, "achieved": achieved, "peak": peak_sus,
+                     "unit": "TFLOP/s", "frac": achieved / peak_sus,
+                     "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a multi-second loop)",
+                     "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
+                     "algorithmic_flop_per_launch": flop, "avg_launch_ms": gemm_avg,
+                     "traffic": kernel_traffic(GEMM_KERNEL)},
+        "hbm_pass": {"kernel": STRIP_KERNEL, "bound": "hbm", "achieved": strip_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": (strip_gbs / peaks["hbm_gbs"]) if strip_gbs else None,
+                     "algorithmic_bytes_per_launch": strip_bytes, "avg_launch_ms": strip_avg},
+        "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in kernels.items()},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
+        "cpu_baseline": {"value": cpu_rate, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                         "sample": f"{n_l} of {L_t} target layers x 4096 tokens, float64, scaled to a full map",
+                         "seconds": cpu_s},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=("full", "small"), default="full",
+                    help="small: T=4096 with the same layer shapes (for profiler captures)")
+    ap.add_argument("--skip-extras", action="store_true", help="skip the end-to-end and CPU-baseline legs")
+    args = ap.parse_args()
+    if args.workload == "small":
+        W["T"] = 4096
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    run_gpu(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

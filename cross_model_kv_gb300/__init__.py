@@ -24,6 +24,8 @@ from ._binding import (  # noqa: F401
     kvb_stats_count,
     kvb_stats_create,
     kvb_stats_destroy,
+    kvb_stats_export,
+    kvb_stats_import,
     kvb_stats_reset,
     kvb_version,
     load_library,

@@ -64,6 +64,8 @@ SIGNATURES = {
     "kvb_stats_reset": (ctypes.c_int, [_P, _P]),
     "kvb_stats_accumulate": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int32, _P]),
     "kvb_stats_count": (ctypes.c_int, [_P, _I64P, _P]),
+    "kvb_stats_export": (ctypes.c_int, [_P, ctypes.c_int32, _I64P, _P, _P, _P, _P, _P, _P]),
+    "kvb_stats_import": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P, _P, _P]),
     "kvb_layer_select": (ctypes.c_int, [_P, _P, ctypes.c_double, _I32P, _I32P, _P, _P]),
     "kvb_ridge_solve": (ctypes.c_int, [_P, _P, _I32P, _I32P, ctypes.c_double, ctypes.c_int, _P, _P, _P, _P, _P]),
 }
@@ -252,6 +254,20 @@ def kvb_stats_count(st: Stats, stream=None) -> int:
     n = ctypes.c_int64()
     _check(load_library().kvb_stats_count(st.handle, ctypes.byref(n), _stream(stream)))
     return int(n.value)
+
+
+def kvb_stats_export(st: Stats, kv: int, mean_x=None, mean_y=None, gram=None, cross=None, syy=None,
+                     stream=None) -> int:
+    """Copy one kv's statistics into the given float32 CUDA tensors; returns n."""
+    n = ctypes.c_int64()
+    _check(load_library().kvb_stats_export(st.handle, int(kv), ctypes.byref(n), _dev(mean_x), _dev(mean_y),
+                                           _dev(gram), _dev(cross), _dev(syy), _stream(stream)))
+    return int(n.value)
+
+
+def kvb_stats_import(st: Stats, kv: int, n_obs: int, mean_x, mean_y, gram, cross, syy, stream=None):
+    _check(load_library().kvb_stats_import(st.handle, int(kv), int(n_obs), _dev(mean_x), _dev(mean_y), _dev(gram),
+                                           _dev(cross), _dev(syy), _stream(stream)))
 
 
 def kvb_layer_select(ctx: Ctx, st: Stats, lam: float = 0.01, r2=None, stream=None):

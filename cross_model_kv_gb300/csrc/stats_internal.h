@@ -1,0 +1,83 @@
+// Internal declarations of the statistics, selection and ridge-solve kernels.
+#pragma once
+
+#include "kvb_internal.h"
+
+namespace kvb {
+
+// Four running-mean vectors: source keys, source values, target keys, target values.
+struct MeanSet {
+    float* mean[4];
+    const float* bmean[4];
+    float* delta[4];
+    int64_t len[4];
+};
+
+cudaError_t launch_select_rows(const int* pos, int64_t T, int stride, int max_pos, int* rows, int* nb, DevErr err,
+                               cudaStream_t s);
+cudaError_t launch_colmean(kvb_dtype dt, const void* cache, int64_t n_slabs, int64_t T, int d, const int* rows,
+                           const int* nb, const int* pos, const float2* tab, bool strip, float* mean,
+                           cudaStream_t s);
+// out_lo == nullptr: float32 output; otherwise the (hi, lo) bf16 split into out / out_lo.
+cudaError_t launch_center_transpose(kvb_dtype dt, const void* cache, int64_t n_slabs, int64_t T, int d,
+                                    const int* rows, const int* nb, const int* pos, const float2* tab, bool strip,
+                                    const float* mean, void* out, void* out_lo, int64_t ld, cudaStream_t s);
+cudaError_t launch_chan_prepare(const MeanSet& ms, const long long* n_dev, const int* nb, float* f,
+                                cudaStream_t s);
+cudaError_t launch_symmetrize(const float* src, float* dst, int64_t n, cudaStream_t s);
+cudaError_t launch_chan_finish(long long* n_dev, const int* nb, cudaStream_t s);
+cudaError_t launch_syy(const void* Y, const void* Ylo, int64_t ld, int64_t rows_n, const int* nb, const float* dy,
+                       const float* f, float* syy, cudaStream_t s);
+cudaError_t launch_stats_gemm_simt(const float* A, const float* B, int64_t ld, int64_t Ma, int64_t Nb, bool lower,
+                                   const float* da, const float* db, const float* f, const int* nb, float* out,
+                                   int64_t ldo, cudaStream_t s);
+
+// Statistics GEMM jobs, K = observations:
+//   out[i][j] += sum_r A[i][r] B[j][r] + f da[i] db[j].
+// CUDA-core path: A, B float32 [rows][ld].  Tensor-core path: A = A + A_lo and
+// B = B + B_lo as bf16 pairs; the product is taken as A.B + A.B_lo + A_lo.B
+// (three bf16 passes into one fp32 accumulator; A_lo.B_lo is below fp32 noise).
+struct StatsJob {
+    const void* A;   // [Ma][ld]
+    const void* B;   // [Nb][ld]
+    const void* A_lo;
+    const void* B_lo;
+    float* out;      // [Ma][ldo]
+    const float* da;
+    const float* db;
+    int64_t Ma, Nb, ldo;
+    int lower;       // only tiles touching the lower triangle (j <= i)
+};
+struct StatsGemmPlan;  // device tile list, built once per statistics object
+bool stats_gemm_tc_supported(const StatsJob* jobs, int n_jobs);
+cudaError_t stats_gemm_tc_plan(const StatsJob* jobs, int n_jobs, StatsGemmPlan** plan);
+void stats_gemm_tc_free(StatsGemmPlan* plan);
+cudaError_t launch_stats_gemm_tc(StatsGemmPlan* plan, const StatsJob* jobs, int n_jobs, int64_t ld,
+                                 const float* f, const int* nb, DevErr err, int num_sms, cudaStream_t s,
+                                 std::string* why);
+
+// ---------------------------------------------------------------- dense solves (fp32, batched)
+// C[b] = alpha * op(A[b]) op(B[b]) + beta * C[b];  A(m,k) = A[m*sam + k*sak],
+// B(k,n) = B[k*sbk + n*sbn], C(m,n) = C[m*ldc + n].  lower: skip tiles above the diagonal.
+struct GemmArgs {
+    const float* A;
+    const float* B;
+    float* C;
+    int64_t sam, sak, sbk, sbn, ldc;
+    int64_t strideA, strideB, strideC;  // per batch item
+    int64_t M, N, K;
+    float alpha, beta;
+    int batch;
+    int lower;
+};
+cudaError_t launch_gemm_f32(const GemmArgs& g, cudaStream_t s);
+
+// In-place Cholesky of batch SPD matrices (lower triangle used), then in-place
+// solve of G X = C for m right-hand sides.  A non-positive pivot records
+// DEV_ERR_NUMERIC in *numeric_flag.
+cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t n, int batch, int* numeric_flag,
+                                cudaStream_t s);
+cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int64_t n, float* C, int64_t ldc,
+                               int64_t strideC, int64_t m, int batch, cudaStream_t s);
+
+}  // namespace kvb

@@ -173,6 +173,22 @@ kvb_status kvb_stats_accumulate(kvb_ctx* ctx, kvb_stats* st, const void* src_k, 
 kvb_status kvb_stats_count(kvb_stats* st, int64_t* n_obs, void* stream);
 
 /*
+ * Checkpoint and inspection of the statistics of one kv (0 = K, 1 = V):
+ * device float32 buffers mean_x [L_src*H*d], mean_y [L_tgt*H*d], gram
+ * [L_src*H*d]^2 (full symmetric matrix), cross [L_src*H*d][L_tgt*H*d], syy
+ * [L_tgt*H*d].  Export: any buffer may be NULL to skip it; n_obs (host, may
+ * be NULL) receives the count and makes the call sync `stream`.  Import
+ * replaces the statistics of that kv and sets the shared count to n_obs
+ * (syncs); accumulating afterwards continues with Chan merges, so a fit can
+ * resume from a checkpoint.
+ */
+kvb_status kvb_stats_export(kvb_stats* st, int32_t kv, int64_t* n_obs, float* mean_x, float* mean_y,
+                            float* gram, float* cross, float* syy, void* stream);
+kvb_status kvb_stats_import(kvb_stats* st, int32_t kv, int64_t n_obs, const float* mean_x,
+                            const float* mean_y, const float* gram, const float* cross,
+                            const float* syy, void* stream);
+
+/*
  * Head-averaged single-source R^2 and top-k ("KVBridge" README, "What ships").
  * For each kv in {K, V}, source layer s and target layer t: the ridge fit of
  * target t from source s alone (lambda absolute, centered), per-column
@@ -190,7 +206,8 @@ kvb_status kvb_layer_select(kvb_ctx* ctx, kvb_stats* st, double lambda, int32_t*
  * centered statistics gathered for the selection, W = (M + lambda I)^-1 C and
  * b = ybar - xbar W.  W_k/W_v device [L_tgt][H*d][k*H*d] in w_dtype (float32
  * solve, rounded once on output for KVB_BF16), b_k/b_v device [L_tgt][H*d]
- * float32.  Returns KVB_ERR_NUMERIC if a system is not positive definite.
+ * float32.  Syncs `stream`; returns KVB_ERR_NUMERIC if a system is not
+ * positive definite.
  */
 kvb_status kvb_ridge_solve(kvb_ctx* ctx, kvb_stats* st, const int32_t* sel_k_host,
                            const int32_t* sel_v_host, double lambda, kvb_dtype w_dtype, void* W_k,

@@ -97,3 +97,55 @@ class ApplyCase:
 
 def spec(L, H, d, theta):
     return {"n_layers": L, "n_kv_heads": H, "head_dim": d, "rope_theta": theta}
+
+
+def make_pair(seed, L_s, L_t, H, d, k, T, n_seq, theta_s, theta_t, noise=1e-3, sigma=0.5, positions=None):
+    """Synthetic calibration pair with a hidden cross-layer affine map (composed by the oracle).
+
+    Returns dict(calib=[(src_k, src_v, tgt_k, tgt_v, pos)] * n_seq, holdout=(...), sel_k, sel_v, ...),
+    float64 host arrays.  `positions` (list per sequence) defaults to 0..T-1.
+    """
+    p, q = k * H * d, H * d
+    sel_k = synth.hidden_selection(seed + 1, L_s, L_t, k)
+    sel_v = synth.hidden_selection(seed + 2, L_s, L_t, k)
+    Wk, bk = synth.hidden_weights(seed + 3, L_t, p, q)
+    Wv, bv = synth.hidden_weights(seed + 4, L_t, p, q)
+    seqs = []
+    for i in range(n_seq + 1):
+        pos = np.arange(T) if positions is None else np.asarray(positions[i])
+        Ti = len(pos)
+        ck = synth.content(seed + 100 + i, L_s, H, Ti, d, sigma)
+        cv = synth.content(seed + 200 + i, L_s, H, Ti, d, sigma)
+        nk = synth.noise(seed + 300 + i, (L_t, Ti, q))
+        nv = synth.noise(seed + 400 + i, (L_t, Ti, q))
+        seqs.append(O.synthesize_pair(ck, cv, pos, theta_s, theta_t, sel_k, sel_v, Wk, bk, Wv, bv, nk, nv,
+                                      noise) + (pos,))
+    return dict(calib=seqs[:n_seq], holdout=seqs[n_seq], sel_k=sel_k, sel_v=sel_v, theta_s=theta_s,
+                theta_t=theta_t, L_s=L_s, L_t=L_t, H=H, d=d, k=k)
+
+
+def round_pair(pair, dtype):
+    """Round every cache of a pair to `dtype` (torch dtype); returns host float64 copies of the rounded values."""
+    import torch
+
+    def r(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dtype).to(torch.float64).numpy()
+
+    out = dict(pair)
+    out["calib"] = [tuple(r(x) for x in s[:4]) + (s[4],) for s in pair["calib"]]
+    h = pair["holdout"]
+    out["holdout"] = tuple(r(x) for x in h[:4]) + (h[4],)
+    return out
+
+
+def oracle_full_stats(pair, stride=4):
+    """Oracle centered statistics over ALL source features / target columns, K and V."""
+    XK, XV, YK, YV = [], [], [], []
+    for src_k, src_v, tgt_k, tgt_v, pos in pair["calib"]:
+        keep = O.retain_stride(pos, stride)
+        XK.append(O.all_layer_features(src_k, pos, pair["theta_s"])[keep])
+        XV.append(O.all_layer_features(src_v)[keep])
+        YK.append(O.all_layer_features(tgt_k, pos, pair["theta_t"])[keep])
+        YV.append(O.all_layer_features(tgt_v)[keep])
+    cat = lambda a: np.concatenate(a, axis=0)
+    return O.centered_stats(cat(XK), cat(YK)), O.centered_stats(cat(XV), cat(YV))

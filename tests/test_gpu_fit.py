@@ -1,0 +1,154 @@
+"""GPU parity of the fit path (statistics, selection, ridge) against the float64 oracle."""
+import numpy as np
+import pytest
+
+import oracle as O
+from cases import TOL_F32, TOL_W, make_pair, oracle_full_stats, rel_fro, round_pair, spec, to_host64
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvb():
+    from cross_model_kv_gb300 import build
+    build.build()
+    import cross_model_kv_gb300 as m
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return m
+
+
+def _dev(a, dtype):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda", dtype)
+
+
+def _accumulate(kvb, ctx, st, seqs, dtype, stride=4):
+    for src_k, src_v, tgt_k, tgt_v, pos in seqs:
+        kvb.kvb_stats_accumulate(ctx, st, _dev(src_k, dtype), _dev(src_v, dtype), _dev(tgt_k, dtype),
+                                 _dev(tgt_v, dtype), _dev(pos.astype(np.int32), torch.int32), stride)
+
+
+def _export(kvb, st, kv, Fs, Ft):
+    f = lambda *s: torch.empty(s, dtype=torch.float32, device="cuda")
+    mx, my, g, c, y = f(Fs), f(Ft), f(Fs, Fs), f(Fs, Ft), f(Ft)
+    n = kvb.kvb_stats_export(st, kv, mx, my, g, c, y)
+    return n, to_host64(mx), to_host64(my), to_host64(g), to_host64(c), to_host64(y)
+
+
+def _ctx(kvb, pair, max_pos):
+    return kvb.kvb_ctx_create(spec(pair["L_s"], pair["H"], pair["d"], pair["theta_s"]),
+                              spec(pair["L_t"], pair["H"], pair["d"], pair["theta_t"]), pair["k"], max_pos)
+
+
+def _check_stats(kvb, st, pair, tol):
+    q = pair["H"] * pair["d"]
+    Fs, Ft = pair["L_s"] * q, pair["L_t"] * q
+    ref = oracle_full_stats(pair)
+    for kv in (0, 1):
+        n, mx, my, g, c, y = _export(kvb, st, kv, Fs, Ft)
+        o = ref[kv]
+        assert n == o.n
+        assert rel_fro(mx, o.xbar) < tol and rel_fro(my, o.ybar) < tol
+        assert rel_fro(g, o.M) < tol, rel_fro(g, o.M)
+        assert rel_fro(c, o.C) < tol, rel_fro(c, o.C)
+        assert rel_fro(y, o.syy) < tol
+
+
+def _run_fit(kvb, ctx, st, pair, w_dtype):
+    L_t, k, q = pair["L_t"], pair["k"], pair["H"] * pair["d"]
+    r2 = torch.empty((2, L_t, pair["L_s"]), dtype=torch.float32, device="cuda")
+    sel_k, sel_v = kvb.kvb_layer_select(ctx, st, 0.01, r2)
+    Wk = torch.empty((L_t, q, k * q), dtype=w_dtype, device="cuda")
+    Wv = torch.empty_like(Wk)
+    bk = torch.empty((L_t, q), dtype=torch.float32, device="cuda")
+    bv = torch.empty_like(bk)
+    kvb.kvb_ridge_solve(ctx, st, sel_k, sel_v, 0.01, Wk, Wv, bk, bv)
+    return sel_k, sel_v, to_host64(r2), Wk, Wv, bk, bv
+
+
+def _check_fit(kvb, ctx, st, pair, w_dtype, w_tol):
+    fit = O.fit_mapper(pair["calib"], pair["theta_s"], pair["theta_t"], pair["k"], 0.01, 4)
+    sel_k, sel_v, r2, Wk, Wv, bk, bv = _run_fit(kvb, ctx, st, pair, w_dtype)
+    assert np.array_equal(sel_k, fit.sel_k) and np.array_equal(sel_v, fit.sel_v)
+    assert np.array_equal(fit.sel_k, pair["sel_k"]) and np.array_equal(fit.sel_v, pair["sel_v"])
+    assert np.max(np.abs(r2[0] - fit.r2_k)) < 1e-4 and np.max(np.abs(r2[1] - fit.r2_v)) < 1e-4
+    gWk = np.transpose(to_host64(Wk), (0, 2, 1))
+    gWv = np.transpose(to_host64(Wv), (0, 2, 1))
+    ek, ev = rel_fro(gWk, fit.W_k), rel_fro(gWv, fit.W_v)
+    assert ek <= w_tol and ev <= w_tol, (ek, ev)
+    assert rel_fro(to_host64(bk), fit.b_k) <= w_tol and rel_fro(to_host64(bv), fit.b_v) <= w_tol
+    return fit, (sel_k, sel_v, Wk, Wv, bk, bv)
+
+
+def test_tiny_pair_fp32_fit_matches_oracle_and_recovers(kvb):
+    # tiny pair: 4 -> 6 layers, 2 KV heads, head_dim 16, k = 2, theta 1e4 -> 5e4,
+    # 4 calibration sequences x 256 tokens, stride 4, noise 1e-3
+    pair = make_pair(0, 4, 6, 2, 16, 2, 256, 4, 1e4, 5e4)
+    ctx = _ctx(kvb, pair, 256)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 256)
+    _accumulate(kvb, ctx, st, pair["calib"], torch.float32)
+    assert kvb.kvb_stats_count(st) == 256
+    _check_stats(kvb, st, pair, 1e-5)
+    fit, (sel_k, sel_v, Wk, Wv, bk, bv) = _check_fit(kvb, ctx, st, pair, torch.float32, 1e-4)
+    # apply the GPU-fitted mapper on the held-out sequence
+    src_k, src_v, tgt_k, tgt_v, pos = pair["holdout"]
+    out_k = torch.empty((6, 2, 256, 16), dtype=torch.float32, device="cuda")
+    out_v = torch.empty_like(out_k)
+    kvb.kvb_map_apply(ctx, _dev(src_k, torch.float32), _dev(src_v, torch.float32),
+                      _dev(pos.astype(np.int32), torch.int32), sel_k, sel_v, Wk, Wv, bk, bv, out_k, out_v)
+    ok, ov = O.map_apply(src_k, src_v, pos, fit.sel_k, fit.sel_v, fit.W_k, fit.b_k, fit.W_v, fit.b_v, 1e4, 5e4, 2, 16)
+    assert rel_fro(to_host64(out_k), ok) < TOL_F32 and rel_fro(to_host64(out_v), ov) < TOL_F32
+    for t in range(6):
+        for a, b in ((tgt_k[t], to_host64(out_k)[t]), (tgt_v[t], to_host64(out_v)[t])):
+            A = np.transpose(a, (1, 0, 2)).reshape(256, 32)
+            B = np.transpose(b, (1, 0, 2)).reshape(256, 32)
+            assert O.head_pooled_r2(A, B, 2, 16) > 0.9999
+
+
+def test_chan_merge_over_ragged_batches_and_offsets(kvb):
+    # unequal batch lengths, positions not starting at 0: merges must equal two-pass statistics
+    rng = np.random.default_rng(3)
+    positions = [np.arange(o, o + n) for o, n in ((0, 64), (5, 200), (17, 33), (100, 128), (0, 10))]
+    pair = make_pair(7, 3, 2, 2, 16, 2, None, 4, 1e4, 1e6, positions=positions)
+    ctx = _ctx(kvb, pair, 512)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 256)
+    _accumulate(kvb, ctx, st, pair["calib"], torch.float32)
+    _check_stats(kvb, st, pair, 1e-5)
+
+
+def test_checkpoint_export_import_resume(kvb):
+    pair = make_pair(9, 3, 2, 2, 16, 2, 128, 4, 1e4, 1e6)
+    q = 32
+    Fs, Ft = 3 * q, 2 * q
+    ctx = _ctx(kvb, pair, 128)
+    a = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 128)
+    _accumulate(kvb, ctx, a, pair["calib"][:2], torch.float32)
+    b = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 128)
+    f = lambda *s: torch.empty(s, dtype=torch.float32, device="cuda")
+    for kv in (0, 1):
+        bufs = (f(Fs), f(Ft), f(Fs, Fs), f(Fs, Ft), f(Ft))
+        n = kvb.kvb_stats_export(a, kv, *bufs)
+        kvb.kvb_stats_import(b, kv, n, *bufs)
+    _accumulate(kvb, ctx, b, pair["calib"][2:], torch.float32)
+    _check_stats(kvb, b, pair, 1e-5)
+
+
+def test_bf16_fit_matches_oracle(kvb):
+    # bf16 caches, head_dim 128: 4 -> 3 layers, 2 KV heads, k = 2, 8 sequences x 1024 tokens
+    pair = round_pair(make_pair(11, 4, 3, 2, 128, 2, 1024, 8, 1e4, 1e6, noise=1e-2, sigma=1.0), torch.bfloat16)
+    ctx = _ctx(kvb, pair, 1024)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, 1024)
+    _accumulate(kvb, ctx, st, pair["calib"], torch.bfloat16)
+    assert kvb.kvb_stats_count(st) == 2048
+    _check_stats(kvb, st, pair, 1e-4)
+    _check_fit(kvb, ctx, st, pair, torch.float32, TOL_W)
+
+
+def test_bad_calibration_position_is_reported(kvb):
+    pair = make_pair(13, 3, 2, 2, 16, 2, 64, 1, 1e4, 1e6)
+    ctx = _ctx(kvb, pair, 32)  # positions reach 63 >= max_pos
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 64)
+    _accumulate(kvb, ctx, st, pair["calib"], torch.float32)
+    with pytest.raises(kvb.KvbError):
+        kvb.kvb_ctx_check(ctx)

@@ -178,6 +178,118 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- fit leg
+
+FIT = dict(L_s=40, L_t=64, H=8, d=128, k=8, seq_len=1024, n_seq=256, batch_tokens=8192, stride=4, theta=1e6,
+           lam=0.01, snr=10.0)
+
+
+FIT_SMALL = dict(FIT, L_s=8, L_t=8, k=4, n_seq=32)
+
+
+def run_fit(kvb, dev, seed=101, small=False):
+    """Calibration statistics + selection + ridge solve, Qwen3-14B->32B shapes.
+
+    256 sequences x 1024 tokens (positions 0..1023) streamed in 32 batches of
+    8192 tokens, stride 4 -> 65,536 observations.  Batch data: source caches
+    drawn with the synthetic recipe; target caches produced from them by a
+    hidden top-8 affine map (applied with kvb_map_apply) plus noise at SNR 10.
+    Four distinct batches are generated and cycled (timing does not depend on
+    the values).  Returns a dict for the JSON line.
+    """
+    import torch
+    import synth
+
+    F = FIT_SMALL if small else FIT
+    L_s, L_t, H, d, k = F["L_s"], F["L_t"], F["H"], F["d"], F["k"]
+    Tb = F["batch_tokens"]
+    q, p = H * d, k * H * d
+    n_batches = F["n_seq"] * F["seq_len"] // Tb
+    spec = lambda L: {"n_layers": L, "n_kv_heads": H, "head_dim": d, "rope_theta": F["theta"]}
+    ctx = kvb.kvb_ctx_create(spec(L_s), spec(L_t), k, F["seq_len"], dev.index or 0)
+    sel_k = synth.hidden_selection(seed + 1, L_s, L_t, k)
+    sel_v = synth.hidden_selection(seed + 2, L_s, L_t, k)
+    Wk, bk = synth.torch_weights(seed + 3, L_t, p, q, torch.bfloat16, dev)
+    Wv, bv = synth.torch_weights(seed + 4, L_t, p, q, torch.bfloat16, dev)
+    pos = torch.arange(F["seq_len"], dtype=torch.int32, device=dev).repeat(Tb // F["seq_len"])
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    sk = torch.empty((L_s, H, Tb, d), dtype=torch.bfloat16, device=dev)
+    sv = torch.empty_like(sk)
+    tk = torch.empty((L_t, H, Tb, d), dtype=torch.bfloat16, device=dev)
+    tv = torch.empty_like(tk)
+
+    def make_batch(b):
+        sk.copy_(synth.torch_content(seed + 10 + b, L_s, H, Tb, d, 1.0, torch.bfloat16, dev))
+        sv.copy_(synth.torch_content(seed + 1000 + b, L_s, H, Tb, d, 1.0, torch.bfloat16, dev))
+        kvb.kvb_map_apply(ctx, sk, sv, pos, sel_k, sel_v, Wk, Wv, bk, bv, tk, tv)
+        for t in (tk, tv):
+            for l in range(L_t):
+                x = t[l].float()
+                x += torch.randn(x.shape, generator=g, device=dev) * (x.std(dim=1, keepdim=True) / F["snr"] ** 0.5)
+                t[l].copy_(x)
+
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, Tb)
+    stream = torch.cuda.current_stream(dev)
+    kvb.kvb_profile_read(ctx)
+    stats_ms = 0.0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kern = {}
+    for b in range(n_batches):  # every batch distinct; only the accumulate calls are timed
+        make_batch(b)
+        kvb.kvb_profile_enable(ctx, True)
+        e0.record(stream)
+        kvb.kvb_stats_accumulate(ctx, st, sk, sv, tk, tv, pos, F["stride"], stream)
+        e1.record(stream)
+        kvb.kvb_profile_enable(ctx, False)
+        torch.cuda.synchronize(dev)
+        stats_ms += e0.elapsed_time(e1)
+        for n, (c, t) in kvb.kvb_profile_read(ctx).items():
+            c0, t0_ = kern.get(n, (0, 0.0))
+            kern[n] = (c0 + c, t0_ + t)
+    del Wk, Wv, sk, sv, tk, tv
+    kvb.kvb_ctx_check(ctx, stream)
+    n_obs = kvb.kvb_stats_count(st, stream)
+    r2 = torch.empty((2, L_t, L_s), dtype=torch.float32, device=dev)
+    kvb.kvb_profile_enable(ctx, True)
+    t0 = time.perf_counter()
+    gk, gv = kvb.kvb_layer_select(ctx, st, F["lam"], r2, stream)
+    t_sel = time.perf_counter() - t0
+    Wk_o = torch.empty((L_t, q, p), dtype=torch.bfloat16, device=dev)
+    Wv_o = torch.empty_like(Wk_o)
+    bk_o = torch.empty((L_t, q), dtype=torch.float32, device=dev)
+    bv_o = torch.empty_like(bk_o)
+    t0 = time.perf_counter()
+    kvb.kvb_ridge_solve(ctx, st, gk, gv, F["lam"], Wk_o, Wv_o, bk_o, bv_o, stream)
+    t_ridge = time.perf_counter() - t0
+    kvb.kvb_profile_enable(ctx, False)
+    for n, (c, t) in kvb.kvb_profile_read(ctx).items():
+        kern[n] = (c, t)
+    Fs, Ft = L_s * q, L_t * q
+    flop_alg = 2 * n_obs * (Fs * Fs / 2 + Fs * Ft) * 2       # lower Gram + cross, K and V
+    gemm_name = "stats_gemm_tcgen05" if "stats_gemm_tcgen05" in kern else "stats_gemm_simt"
+    gemm_n, gemm_ms = kern.get(gemm_name, (0, 0.0))
+    gather_n, gather_ms = kern.get("calib_gather_center", (0, 0.0))
+    nb = Tb // F["stride"]
+    # algorithmic bytes: kept rows of the four caches read once, centered (hi, lo) operands written once
+    gather_bytes = n_batches * ((2 * L_s + 2 * L_t) * H * nb * d * 2 + (2 * Fs + 2 * Ft) * nb * 4)
+    out = {"workload": (f"{L_s}->{L_t} layers, k={k}, " if small else "qwen3-14b->32b-shaped fit: ") +
+                       f"{F['n_seq']} x {F['seq_len']} calibration tokens in {n_batches} batches of {Tb}, stride 4, "
+                       "bf16 caches, fp32 statistics (split-bf16 tensor-core products), lambda 0.01",
+           "n_obs": n_obs, "batches": n_batches,
+           "stats_ms": stats_ms, "stats_gemm_kernel": gemm_name, "stats_gemm_ms": gemm_ms,
+           "stats_gemm_tflops_algorithmic": flop_alg / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
+           "stats_gemm_tflops_executed": 3 * flop_alg / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
+           "gather_ms": gather_ms, "gather_gbs": gather_bytes / (gather_ms / 1e3) / 1e9 if gather_ms else None,
+           "select_s": t_sel, "ridge_s": t_ridge,
+           "selection_recovered": float((np.asarray(gk) == sel_k).mean() + (np.asarray(gv) == sel_v).mean()) / 2,
+           "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in kern.items()}}
+    del st, Wk_o, Wv_o
+    kvb.kvb_ctx_destroy(ctx)
+    torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args, rank, world, local_rank):
@@ -293,6 +405,24 @@ def run_gpu(args, rank, world, local_rank):
     kvb.kvb_ctx_check(ctx, stream)
     del h_src_k, h_src_v, h_out_k, h_out_v
 
+    # host copy of a bounded sample of the workload for the CPU baseline (rank 0 only)
+    n_l, T_cpu = 4, 4096
+    sample = None
+    if rank == 0:
+        tok = torch.arange(0, T_cpu, dtype=torch.int64, device=dev)
+        li = torch.arange(n_l, device=dev)
+        hs = lambda x: x.to(dtype=torch.float64).cpu().numpy()
+        sample = (hs(src_k.index_select(2, tok)), hs(src_v.index_select(2, tok)), np.arange(T_cpu), sel_k, sel_v,
+                  np.transpose(hs(W_k.index_select(0, li)), (0, 2, 1)), hs(b_k.index_select(0, li)),
+                  np.transpose(hs(W_v.index_select(0, li)), (0, 2, 1)), hs(b_v.index_select(0, li)))
+    del src_k, src_v, out_k, out_v, W_k, W_v
+    kvb.kvb_ctx_destroy(ctx)
+    torch.cuda.empty_cache()
+
+    fit = None
+    if not args.skip_fit:
+        fit = run_fit(kvb, dev)
+
     if rank != 0:
         return
 
@@ -307,14 +437,7 @@ def run_gpu(args, rank, world, local_rank):
     strip_bytes = 2 * (L_s * H * T * d * 2)
     strip_gbs = strip_bytes / (strip_avg / 1000.0) / 1e9 if strip_avg > 0 else None
 
-    # ---------------- CPU baseline: the oracle, bounded sample of the same workload (rank 0 only)
-    tok = torch.arange(0, 4096, dtype=torch.int64, device=dev)
-    n_l = 4
-    li = torch.arange(n_l, device=dev)
-    hs = lambda x: x.to(dtype=torch.float64).cpu().numpy()
-    sample = (hs(src_k.index_select(2, tok)), hs(src_v.index_select(2, tok)), np.arange(4096), sel_k, sel_v,
-              np.transpose(hs(W_k.index_select(0, li)), (0, 2, 1)), hs(b_k.index_select(0, li)),
-              np.transpose(hs(W_v.index_select(0, li)), (0, 2, 1)), hs(b_v.index_select(0, li)))
+    # ---------------- CPU baseline: the oracle on the bounded sample taken above
     cpu_rate, cpu_s = oracle_rate(*sample, np.arange(n_l))
 
     line = {
@@ -338,8 +461,9 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
+        "fit": fit,
         "cpu_baseline": {"value": cpu_rate, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
-                         "sample": f"{n_l} of {L_t} target layers x 4096 tokens, float64, scaled to a full map",
+                         "sample": f"{n_l} of {L_t} target layers x {T_cpu} tokens, float64, scaled to a full map",
                          "seconds": cpu_s},
     }
     print(json.dumps(line), flush=True)
@@ -353,7 +477,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=("full", "small"), default="full",
                     help="small: T=4096 with the same layer shapes (for profiler captures)")
-    ap.add_argument("--skip-extras", action="store_true", help="skip the end-to-end and CPU-baseline legs")
+    ap.add_argument("--skip-extras", action="store_true", help="skip the end-to-end, fit and CPU-baseline legs")
+    ap.add_argument("--skip-fit", action="store_true", help="skip the calibration-statistics / fit leg")
+    ap.add_argument("--fit-only", action="store_true", help="run only the fit leg (with --workload small: 8 -> 8 layers)")
     args = ap.parse_args()
     if args.workload == "small":
         W["T"] = 4096
@@ -364,6 +490,17 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.fit_only:
+        import torch
+        from cross_model_kv_gb300 import build as kbuild
+        kbuild.build()
+        import cross_model_kv_gb300 as kvb
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        fit = run_fit(kvb, dev, small=args.workload == "small")
+        if rank == 0:
+            print(json.dumps({"fit": fit}), flush=True)
         return
     if world > 1:
         import torch

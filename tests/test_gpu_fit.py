@@ -135,11 +135,14 @@ def test_checkpoint_export_import_resume(kvb):
 
 
 def test_bf16_fit_matches_oracle(kvb):
-    # bf16 caches, head_dim 128: 4 -> 3 layers, 2 KV heads, k = 2, 8 sequences x 1024 tokens
+    # bf16 caches, head_dim 128: 4 -> 3 layers, 2 KV heads, k = 2, 8 sequences x 1024 tokens;
+    # 1024 source features x 768 target columns tile by 128 x 256: tensor-core statistics
     pair = round_pair(make_pair(11, 4, 3, 2, 128, 2, 1024, 8, 1e4, 1e6, noise=1e-2, sigma=1.0), torch.bfloat16)
     ctx = _ctx(kvb, pair, 1024)
     st = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, 1024)
+    kvb.kvb_profile_enable(ctx, True)
     _accumulate(kvb, ctx, st, pair["calib"], torch.bfloat16)
+    assert kvb.kvb_profile_read(ctx)["stats_gemm_tcgen05"][0] == 8
     assert kvb.kvb_stats_count(st) == 2048
     _check_stats(kvb, st, pair, 1e-4)
     _check_fit(kvb, ctx, st, pair, torch.float32, TOL_W)
@@ -152,3 +155,14 @@ def test_bad_calibration_position_is_reported(kvb):
     _accumulate(kvb, ctx, st, pair["calib"], torch.float32)
     with pytest.raises(kvb.KvbError):
         kvb.kvb_ctx_check(ctx)
+
+
+def test_bf16_fit_cuda_core_statistics_path(kvb):
+    # head_dim 64 and 3 target layers: 384 target columns do not tile by 256, so the
+    # statistics run on the CUDA-core kernel (float32 centered operands)
+    pair = round_pair(make_pair(12, 3, 3, 2, 64, 2, 512, 8, 1e4, 1e6, noise=1e-2, sigma=1.0), torch.bfloat16)
+    ctx = _ctx(kvb, pair, 512)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, 512)
+    _accumulate(kvb, ctx, st, pair["calib"], torch.bfloat16)
+    _check_stats(kvb, st, pair, 1e-5)
+    _check_fit(kvb, ctx, st, pair, torch.bfloat16, 5e-3)

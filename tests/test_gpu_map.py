@@ -28,8 +28,12 @@ def _ctx(kvb, c, max_pos):
 
 def _check_all(kvb, c, max_pos, tol, layers=None, tokens=None):
     ctx = _ctx(kvb, c, max_pos)
+    kvb.kvb_profile_enable(ctx, True)
     c.run(kvb, ctx)
     kvb.kvb_ctx_check(ctx)
+    ran = kvb.kvb_profile_read(ctx)
+    tensor_core = c.dtype == torch.bfloat16 and c.d == 128 and (c.H * c.d) % 256 == 0
+    assert ("map_gemm_tcgen05" in ran) == tensor_core and ("map_simt" in ran) != tensor_core, ran
     ok, ov = c.oracle(layers, tokens)
     gk, gv = c.gpu(layers, tokens)
     ek, ev = rel_fro(gk, ok), rel_fro(gv, ov)

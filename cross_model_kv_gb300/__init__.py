@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     kvb_ctx_reserve,
     kvb_layer_select,
     kvb_map_apply,
+    kvb_map_apply_noalloc,
     kvb_model_spec,
     kvb_profile_enable,
     kvb_profile_read,

@@ -59,6 +59,8 @@ SIGNATURES = {
     "kvb_profile_read": (ctypes.c_int, [_P, ctypes.POINTER(kvb_kernel_time), ctypes.c_int32, _I32P]),
     "kvb_map_apply": (ctypes.c_int, [_P, ctypes.c_int, _P, _P, _P, ctypes.c_int64, _I32P, _I32P, _P, _P, _P, _P,
                                      _P, _P, _P]),
+    "kvb_map_apply_noalloc": (ctypes.c_int, [_SPEC_P, _SPEC_P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P,
+                                             ctypes.c_int64, _I32P, _I32P, _P, _P, _P, _P, _P, _P, _P]),
     "kvb_stats_create": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.POINTER(_P)]),
     "kvb_stats_destroy": (ctypes.c_int, [_P]),
     "kvb_stats_reset": (ctypes.c_int, [_P, _P]),
@@ -213,6 +215,25 @@ def kvb_map_apply(ctx: Ctx, src_k, src_v, positions, sel_k, sel_v, W_k, W_v, b_k
     sv = _host_sel(sel_v, ctx.L_t, ctx.k)
     _check(load_library().kvb_map_apply(
         ctx.handle, _dtype_of(src_k), _dev(src_k), _dev(src_v), _dev(positions), T,
+        sk.ctypes.data_as(_I32P), sv.ctypes.data_as(_I32P), _dev(W_k), _dev(W_v), _dev(b_k), _dev(b_v),
+        _dev(out_k), _dev(out_v), _stream(stream)))
+
+
+def kvb_map_apply_noalloc(src, tgt, top_k: int, max_pos: int, src_k, src_v, positions, sel_k, sel_v, W_k, W_v,
+                          b_k, b_v, out_k, out_v, stream=None):
+    """kvb_map_apply without a context and without any device allocation.
+
+    For callers that may not allocate device memory (e.g. inside another
+    framework's memory pool): the scratch lives in a fixed 64 MiB array of the
+    library.  Calls share that array, so they must not overlap on the GPU.
+    """
+    s, t = _spec(src), _spec(tgt)
+    L_t = t.n_layers
+    T = int(src_k.shape[2])
+    sk = _host_sel(sel_k, L_t, int(top_k))
+    sv = _host_sel(sel_v, L_t, int(top_k))
+    _check(load_library().kvb_map_apply_noalloc(
+        ctypes.byref(s), ctypes.byref(t), int(top_k), int(max_pos), _dev(src_k), _dev(src_v), _dev(positions), T,
         sk.ctypes.data_as(_I32P), sv.ctypes.data_as(_I32P), _dev(W_k), _dev(W_v), _dev(b_k), _dev(b_v),
         _dev(out_k), _dev(out_v), _stream(stream)))
 

@@ -142,6 +142,35 @@ kvb_status kvb_map_apply(kvb_ctx* ctx, kvb_dtype dtype, const void* src_k, const
                          const float* b_v, void* out_k, void* out_v, void* stream);
 
 /*
+ * kvb_map_apply_noalloc -- the pages have no counterpart; this is a deployment
+ * variant of kvb_map_apply for callers that cannot allocate device memory,
+ * such as code running inside another framework's caching allocator or a
+ * runtime that owns the whole device budget: they cannot create a kvb_ctx,
+ * because a context allocates its RoPE tables and strip scratch.
+ *   Same arguments and results as kvb_map_apply (bf16 only, head_dim 128,
+ *   n_kv_heads * 128 a multiple of 256), with the pair described by
+ *   src / tgt / top_k / max_pos instead of a context.  The caller passes
+ *   inputs and outputs; the call allocates nothing.  Its scratch (both RoPE
+ *   tables, the stripped source keys, an error word) lives in a fixed 64 MiB
+ *   array inside the library, held on every GPU that loads the library until
+ *   the process exits.
+ *   Limit: 8*max_pos*head_dim + 2*L_src*n_kv_heads*T*head_dim bytes (plus
+ *   alignment) must fit in 64 MiB, else KVB_ERR_INVALID_ARG; e.g. about 800
+ *   tokens at the Qwen3-14B -> 32B shape with max_pos = T.
+ *   The first call on each device looks up the array's device address with
+ *   cudaGetSymbolAddress; make that first call before capturing a stream.
+ *   Every call reuses the same array, so calls that overlap on the GPU (other
+ *   streams, other host threads) race: serialise them.  The call waits for its
+ *   own kernels on `stream` and returns their errors (bad position, timeout).
+ */
+kvb_status kvb_map_apply_noalloc(const kvb_model_spec* src, const kvb_model_spec* tgt, int32_t top_k,
+                                 int32_t max_pos, const void* src_k, const void* src_v,
+                                 const int32_t* positions, int64_t T, const int32_t* sel_k,
+                                 const int32_t* sel_v, const void* W_k, const void* W_v,
+                                 const float* b_k, const float* b_v, void* out_k, void* out_v,
+                                 void* stream);
+
+/*
  * Calibration statistics ("KVBridge" README, "Loading").  One object holds, for
  * K and for V, the observation count n, the feature and target means, the
  * centered Gram over ALL source features (L_src*H*d square), the centered

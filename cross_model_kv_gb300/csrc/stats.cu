@@ -165,6 +165,162 @@ __global__ void __launch_bounds__(256) center_transpose_kernel(const T* __restri
     }
 }
 
+// ---------------------------------------------------------------------------
+// Vectorised gather for bf16 caches with head_dim % 16 == 0: each lane owns 8
+// contiguous dims of a row (one 16-byte load); the RoPE partner dims of the
+// same row sit in lane ^ (d/16), fetched with a shuffle.  Loops are
+// warp-uniform so the shuffles always see the whole warp.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]);
+        x[2 * q] = f.x;
+        x[2 * q + 1] = f.y;
+    }
+}
+
+// Stripped (keys) or raw (values) features of 8 dims of one kept row.
+__device__ __forceinline__ void load_row8(const __nv_bfloat16* __restrict__ slab_base, bool valid, int tok, int d,
+                                          int sub, int pl, const int* __restrict__ pos,
+                                          const float2* __restrict__ tab, bool strip, float (&y)[8]) {
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (valid) raw = __ldg(reinterpret_cast<const uint4*>(slab_base + static_cast<int64_t>(tok) * d + sub * 8));
+    unpack8(raw, y);
+    if (!strip) return;
+    uint4 pr;
+    pr.x = __shfl_xor_sync(0xffffffffu, raw.x, pl);
+    pr.y = __shfl_xor_sync(0xffffffffu, raw.y, pl);
+    pr.z = __shfl_xor_sync(0xffffffffu, raw.z, pl);
+    pr.w = __shfl_xor_sync(0xffffffffu, raw.w, pl);
+    if (!valid) return;
+    float p[8];
+    unpack8(pr, p);
+    const int half = d >> 1;
+    const bool lo = sub < pl;
+    const int i0 = lo ? sub * 8 : sub * 8 - half;
+    const float4* t4 = reinterpret_cast<const float4*>(tab + static_cast<int64_t>(__ldg(pos + tok)) * half + i0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 cs = __ldg(t4 + q);  // (c, s) of two consecutive pairs
+        const float s0 = lo ? cs.y : -cs.y, s1 = lo ? cs.w : -cs.w;
+        y[2 * q] = fmaf(y[2 * q], cs.x, p[2 * q] * s0);
+        y[2 * q + 1] = fmaf(y[2 * q + 1], cs.z, p[2 * q + 1] * s1);
+    }
+}
+
+// Partial column sums: part[split][slab*d + e] over the split's share of kept rows.
+__global__ void __launch_bounds__(256) colsum_vec_kernel(const __nv_bfloat16* __restrict__ cache, int64_t T_len,
+                                                         int d, const int* __restrict__ rows,
+                                                         const int* __restrict__ nb, const int* __restrict__ pos,
+                                                         const float2* __restrict__ tab, bool strip,
+                                                         float* __restrict__ part, int64_t F) {
+    __shared__ float red[256 * 8];
+    const int slab = blockIdx.x, split = blockIdx.y, S = gridDim.y;
+    const int lpr = d >> 3;           // lanes per row
+    const int rpi = 256 / lpr;        // rows per iteration
+    const int sub = threadIdx.x % lpr;
+    const int rr = threadIdx.x / lpr;
+    const int pl = d >> 4;
+    const int n = *nb;
+    const int chunk = (n + S - 1) / S;
+    const int r0 = split * chunk, r1 = min(n, r0 + chunk);
+    const __nv_bfloat16* base = cache + static_cast<int64_t>(slab) * T_len * d;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int b = r0; b < r1; b += rpi) {
+        const int r = b + rr;
+        const bool valid = r < r1;
+        const int tok = valid ? __ldg(rows + r) : 0;
+        float y[8];
+        load_row8(base, valid, tok, d, sub, pl, pos, tab, strip, y);
+        if (valid) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] += y[i];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red[rr * d + sub * 8 + i] = acc[i];
+    __syncthreads();
+    for (int e = threadIdx.x; e < d; e += blockDim.x) {
+        float s = 0.f;
+        for (int q = 0; q < rpi; ++q) s += red[q * d + e];
+        part[static_cast<int64_t>(split) * F + static_cast<int64_t>(slab) * d + e] = s;
+    }
+}
+
+__global__ void mean_finalize_kernel(const float* __restrict__ part, int S, int64_t F, const int* __restrict__ nb,
+                                     float* __restrict__ mean) {
+    const int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (c >= F) return;
+    const int n = *nb;
+    float s = 0.f;
+    for (int q = 0; q < S; ++q) s += part[q * F + c];
+    mean[c] = n > 0 ? s / static_cast<float>(n) : 0.f;
+}
+
+// Centered, transposed compaction of 64 kept rows of one slab (see
+// center_transpose_kernel), vectorised.  tile[e][r] in shared memory.
+__global__ void __launch_bounds__(256) center_vec_kernel(const __nv_bfloat16* __restrict__ cache, int64_t T_len,
+                                                         int d, const int* __restrict__ rows,
+                                                         const int* __restrict__ nb, const int* __restrict__ pos,
+                                                         const float2* __restrict__ tab, bool strip,
+                                                         const float* __restrict__ mean, void* __restrict__ out,
+                                                         void* __restrict__ out_lo, int64_t ld) {
+    extern __shared__ float tile[];  // [d][65]
+    const int slab = blockIdx.x;
+    const int r0 = blockIdx.y * 64;
+    const int n = *nb;
+    if (r0 >= ((n + 63) & ~63)) return;
+    const int lpr = d >> 3, rpi = 256 / lpr;
+    const int sub = threadIdx.x % lpr, rq = threadIdx.x / lpr;
+    const int pl = d >> 4;
+    const __nv_bfloat16* base = cache + static_cast<int64_t>(slab) * T_len * d;
+    float mu[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mu[i] = mean[static_cast<int64_t>(slab) * d + sub * 8 + i];
+    for (int b = 0; b < 64; b += rpi) {
+        const int rr = b + rq;
+        const int r = r0 + rr;
+        const bool valid = rr < 64 && r < n;
+        const int tok = valid ? __ldg(rows + r) : 0;
+        float y[8];
+        load_row8(base, valid, tok, d, sub, pl, pos, tab, strip, y);
+        if (rr < 64) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) tile[(sub * 8 + i) * 65 + rr] = valid ? y[i] - mu[i] : 0.f;
+        }
+    }
+    __syncthreads();
+    const int64_t row0 = static_cast<int64_t>(slab) * d;
+    if (out_lo == nullptr) {
+        for (int idx = threadIdx.x; idx < d * 16; idx += blockDim.x) {
+            const int e = idx >> 4, q = idx & 15;
+            const float* t = tile + e * 65 + 4 * q;
+            *reinterpret_cast<float4*>(static_cast<float*>(out) + (row0 + e) * ld + r0 + 4 * q) =
+                make_float4(t[0], t[1], t[2], t[3]);
+        }
+    } else {
+        for (int idx = threadIdx.x; idx < d * 8; idx += blockDim.x) {
+            const int e = idx >> 3, q = idx & 7;
+            const float* t = tile + e * 65 + 8 * q;
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat16 h0 = __float2bfloat16_rn(t[2 * j]), h1 = __float2bfloat16_rn(t[2 * j + 1]);
+                const float l0 = t[2 * j] - __bfloat162float(h0), l1 = t[2 * j + 1] - __bfloat162float(h1);
+                __nv_bfloat162 hh(h0, h1);
+                hi[j] = *reinterpret_cast<uint32_t*>(&hh);
+                lo[j] = pack_bf16x2(l0, l1);
+            }
+            const int64_t o = (row0 + e) * ld + r0 + 8 * q;
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_lo) + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+    }
+}
+
 // delta = batch mean - running mean (before the merge); running mean updated;
 // f = n_a n_b / (n_a + n_b).  Thread per column over the four mean vectors.
 __global__ void chan_prepare_kernel(MeanSet ms, const long long* __restrict__ n_dev, const int* __restrict__ nb,
@@ -291,16 +447,26 @@ cudaError_t launch_select_rows(const int* pos, int64_t T, int stride, int max_po
     return cudaGetLastError();
 }
 
+constexpr int kMeanSplits = 8;
+
+bool gather_vec_ok(kvb_dtype dt, int d) { return dt == KVB_BF16 && d % 16 == 0 && d <= 256; }
+
 cudaError_t launch_colmean(kvb_dtype dt, const void* cache, int64_t n_slabs, int64_t T, int d, const int* rows,
-                           const int* nb, const int* pos, const float2* tab, bool strip, float* mean,
+                           const int* nb, const int* pos, const float2* tab, bool strip, float* mean, float* part,
                            cudaStream_t s) {
     if (n_slabs == 0) return cudaSuccess;
-    if (dt == KVB_F32)
+    if (gather_vec_ok(dt, d) && part != nullptr) {
+        const int64_t F = n_slabs * d;
+        colsum_vec_kernel<<<dim3(static_cast<unsigned>(n_slabs), kMeanSplits), 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(cache), T, d, rows, nb, pos, tab, strip, part, F);
+        mean_finalize_kernel<<<static_cast<unsigned>((F + 255) / 256), 256, 0, s>>>(part, kMeanSplits, F, nb, mean);
+    } else if (dt == KVB_F32) {
         colmean_kernel<float><<<static_cast<unsigned>(n_slabs), 256, 0, s>>>(
             static_cast<const float*>(cache), T, d, rows, nb, pos, tab, strip, mean);
-    else
+    } else {
         colmean_kernel<__nv_bfloat16><<<static_cast<unsigned>(n_slabs), 256, 0, s>>>(
             static_cast<const __nv_bfloat16*>(cache), T, d, rows, nb, pos, tab, strip, mean);
+    }
     return cudaGetLastError();
 }
 
@@ -309,6 +475,13 @@ cudaError_t launch_center_transpose(kvb_dtype dt, const void* cache, int64_t n_s
                                     const float* mean, void* out, void* out_lo, int64_t ld, cudaStream_t s) {
     if (n_slabs == 0) return cudaSuccess;
     dim3 grid(static_cast<unsigned>(n_slabs), static_cast<unsigned>((T + 63) / 64));
+    if (gather_vec_ok(dt, d)) {
+        const size_t vsmem = static_cast<size_t>(d) * 65 * sizeof(float);
+        cudaFuncSetAttribute(center_vec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 80 * 1024);
+        center_vec_kernel<<<grid, 256, vsmem, s>>>(static_cast<const __nv_bfloat16*>(cache), T, d, rows, nb, pos, tab,
+                                                   strip, mean, out, out_lo, ld);
+        return cudaGetLastError();
+    }
     const size_t smem = 64 * (d + 1) * sizeof(float);
     if (dt == KVB_F32) {
         cudaFuncSetAttribute(center_transpose_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 80 * 1024);

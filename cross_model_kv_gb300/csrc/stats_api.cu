@@ -26,6 +26,7 @@ struct kvb_stats {
     float* mean[4] = {};   // running means: source K, source V, target K, target V
     float* bmean[4] = {};  // batch means
     float* delta[4] = {};  // batch mean - running mean before the merge
+    float* bpart = nullptr;  // [8][max(Fs, Ft)] partial column sums of one matrix
     float* gram[2] = {};   // [Fs][Fs], lower triangle kept
     float* cross[2] = {};  // [Fs][Ft]
     float* syy[2] = {};    // [Ft]
@@ -197,6 +198,7 @@ kvb_status kvb_stats_create(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_batch_tok
             A(&st->YT[kv], static_cast<size_t>(st->Ft) * st->ld * 4);
         }
     }
+    A(reinterpret_cast<void**>(&st->bpart), 8ull * std::max(st->Fs, st->Ft) * 4);
     A(reinterpret_cast<void**>(&st->r2), 2ull * ctx->L_t * ctx->L_s * 4);
     A(reinterpret_cast<void**>(&st->sel), 2ull * ctx->L_t * ctx->k * 4);
     if (s == KVB_OK) s = zero_stats(st, 0);
@@ -267,7 +269,7 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
         ProfScope ps(c, cs, "calib_gather_center");
         for (int m = 0; m < 4 && e == cudaSuccess; ++m)
             e = launch_colmean(dt, caches[m], slabs[m], T, c->d, st->rows, st->nb_dev, positions, tabs[m],
-                               tabs[m] != nullptr, st->bmean[m], cs);
+                               tabs[m] != nullptr, st->bmean[m], st->bpart, cs);
         MeanSet ms;
         for (int m = 0; m < 4; ++m) {
             ms.mean[m] = st->mean[m];

@@ -15,8 +15,10 @@ struct MeanSet {
 
 cudaError_t launch_select_rows(const int* pos, int64_t T, int stride, int max_pos, int* rows, int* nb, DevErr err,
                                cudaStream_t s);
+// Batch column means.  `part` ([8][n_slabs*d] floats) enables the vectorised
+// bf16 path (head_dim % 16 == 0); NULL forces the generic kernel.
 cudaError_t launch_colmean(kvb_dtype dt, const void* cache, int64_t n_slabs, int64_t T, int d, const int* rows,
-                           const int* nb, const int* pos, const float2* tab, bool strip, float* mean,
+                           const int* nb, const int* pos, const float2* tab, bool strip, float* mean, float* part,
                            cudaStream_t s);
 // out_lo == nullptr: float32 output; otherwise the (hi, lo) bf16 split into out / out_lo.
 cudaError_t launch_center_transpose(kvb_dtype dt, const void* cache, int64_t n_slabs, int64_t T, int d,

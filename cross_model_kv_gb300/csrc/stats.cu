@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(256) center_transpose_kernel(const T* __restri
 // ---------------------------------------------------------------------------
 // Vectorised gather for bf16 caches with head_dim % 16 == 0: each lane owns 8
 // contiguous dims of a row (one 16-byte load); the RoPE partner dims of the
-// same row sit in lane ^ (d/16), fetched with a shuffle.  Loops are
+// same row sit in lane ^ (d/16), fetched with a shuffle.  Each thread handles
+// R rows per step with all their loads issued before any use, so R row loads,
+// position loads and table loads are in flight at once.  Loops are
 // warp-uniform so the shuffles always see the whole warp.
 // ---------------------------------------------------------------------------
 
@@ -182,34 +184,53 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
     }
 }
 
-// Stripped (keys) or raw (values) features of 8 dims of one kept row.
-__device__ __forceinline__ void load_row8(const __nv_bfloat16* __restrict__ slab_base, bool valid, int tok, int d,
-                                          int sub, int pl, const int* __restrict__ pos,
-                                          const float2* __restrict__ tab, bool strip, float (&y)[8]) {
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (valid) raw = __ldg(reinterpret_cast<const uint4*>(slab_base + static_cast<int64_t>(tok) * d + sub * 8));
-    unpack8(raw, y);
-    if (!strip) return;
-    uint4 pr;
-    pr.x = __shfl_xor_sync(0xffffffffu, raw.x, pl);
-    pr.y = __shfl_xor_sync(0xffffffffu, raw.y, pl);
-    pr.z = __shfl_xor_sync(0xffffffffu, raw.z, pl);
-    pr.w = __shfl_xor_sync(0xffffffffu, raw.w, pl);
-    if (!valid) return;
-    float p[8];
-    unpack8(pr, p);
+// Stripped (keys) or raw (values) features of 8 dims of R kept rows.
+template <int R>
+__device__ __forceinline__ void load_rows8(const __nv_bfloat16* __restrict__ slab_base, const bool (&valid)[R],
+                                           const int (&tok)[R], int d, int sub, int pl,
+                                           const int* __restrict__ pos, const float2* __restrict__ tab, bool strip,
+                                           float (&y)[R][8]) {
+    uint4 raw[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u)
+        raw[u] = valid[u] ? __ldg(reinterpret_cast<const uint4*>(slab_base + static_cast<int64_t>(tok[u]) * d + sub * 8))
+                          : make_uint4(0, 0, 0, 0);
+    if (!strip) {
+#pragma unroll
+        for (int u = 0; u < R; ++u) unpack8(raw[u], y[u]);
+        return;
+    }
     const int half = d >> 1;
     const bool lo = sub < pl;
     const int i0 = lo ? sub * 8 : sub * 8 - half;
-    const float4* t4 = reinterpret_cast<const float4*>(tab + static_cast<int64_t>(__ldg(pos + tok)) * half + i0);
+    float4 cs[R][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float4 cs = __ldg(t4 + q);  // (c, s) of two consecutive pairs
-        const float s0 = lo ? cs.y : -cs.y, s1 = lo ? cs.w : -cs.w;
-        y[2 * q] = fmaf(y[2 * q], cs.x, p[2 * q] * s0);
-        y[2 * q + 1] = fmaf(y[2 * q + 1], cs.z, p[2 * q + 1] * s1);
+    for (int u = 0; u < R; ++u) {
+        const int p = valid[u] ? __ldg(pos + tok[u]) : 0;
+        const float4* t4 = reinterpret_cast<const float4*>(tab + static_cast<int64_t>(p) * half + i0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cs[u][q] = __ldg(t4 + q);
+    }
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+        uint4 pr;
+        pr.x = __shfl_xor_sync(0xffffffffu, raw[u].x, pl);
+        pr.y = __shfl_xor_sync(0xffffffffu, raw[u].y, pl);
+        pr.z = __shfl_xor_sync(0xffffffffu, raw[u].z, pl);
+        pr.w = __shfl_xor_sync(0xffffffffu, raw[u].w, pl);
+        float x[8], p[8];
+        unpack8(raw[u], x);
+        unpack8(pr, p);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // cs = (c, s) of two consecutive pairs
+            const float s0 = lo ? cs[u][q].y : -cs[u][q].y, s1 = lo ? cs[u][q].w : -cs[u][q].w;
+            y[u][2 * q] = fmaf(x[2 * q], cs[u][q].x, p[2 * q] * s0);
+            y[u][2 * q + 1] = fmaf(x[2 * q + 1], cs[u][q].z, p[2 * q + 1] * s1);
+        }
     }
 }
+
+constexpr int kRowsPerStep = 4;
 
 // Partial column sums: part[split][slab*d + e] over the split's share of kept rows.
 __global__ void __launch_bounds__(256) colsum_vec_kernel(const __nv_bfloat16* __restrict__ cache, int64_t T_len,
@@ -220,7 +241,7 @@ __global__ void __launch_bounds__(256) colsum_vec_kernel(const __nv_bfloat16* __
     __shared__ float red[256 * 8];
     const int slab = blockIdx.x, split = blockIdx.y, S = gridDim.y;
     const int lpr = d >> 3;           // lanes per row
-    const int rpi = 256 / lpr;        // rows per iteration
+    const int rpi = 256 / lpr;        // rows per row-slot sweep
     const int sub = threadIdx.x % lpr;
     const int rr = threadIdx.x / lpr;
     const int pl = d >> 4;
@@ -229,16 +250,23 @@ __global__ void __launch_bounds__(256) colsum_vec_kernel(const __nv_bfloat16* __
     const int r0 = split * chunk, r1 = min(n, r0 + chunk);
     const __nv_bfloat16* base = cache + static_cast<int64_t>(slab) * T_len * d;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int b = r0; b < r1; b += rpi) {
-        const int r = b + rr;
-        const bool valid = r < r1;
-        const int tok = valid ? __ldg(rows + r) : 0;
-        float y[8];
-        load_row8(base, valid, tok, d, sub, pl, pos, tab, strip, y);
-        if (valid) {
+    for (int b = r0; b < r1; b += rpi * kRowsPerStep) {
+        bool valid[kRowsPerStep];
+        int tok[kRowsPerStep];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] += y[i];
+        for (int u = 0; u < kRowsPerStep; ++u) {
+            const int r = b + u * rpi + rr;
+            valid[u] = r < r1;
+            tok[u] = valid[u] ? __ldg(rows + r) : 0;
         }
+        float y[kRowsPerStep][8];
+        load_rows8<kRowsPerStep>(base, valid, tok, d, sub, pl, pos, tab, strip, y);
+#pragma unroll
+        for (int u = 0; u < kRowsPerStep; ++u)
+            if (valid[u]) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] += y[u][i];
+            }
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) red[rr * d + sub * 8 + i] = acc[i];
@@ -280,16 +308,24 @@ __global__ void __launch_bounds__(256) center_vec_kernel(const __nv_bfloat16* __
     float mu[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) mu[i] = mean[static_cast<int64_t>(slab) * d + sub * 8 + i];
-    for (int b = 0; b < 64; b += rpi) {
-        const int rr = b + rq;
-        const int r = r0 + rr;
-        const bool valid = rr < 64 && r < n;
-        const int tok = valid ? __ldg(rows + r) : 0;
-        float y[8];
-        load_row8(base, valid, tok, d, sub, pl, pos, tab, strip, y);
-        if (rr < 64) {
+    for (int b = 0; b < 64; b += rpi * kRowsPerStep) {
+        bool valid[kRowsPerStep];
+        int tok[kRowsPerStep];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) tile[(sub * 8 + i) * 65 + rr] = valid ? y[i] - mu[i] : 0.f;
+        for (int u = 0; u < kRowsPerStep; ++u) {
+            const int rr = b + u * rpi + rq;
+            valid[u] = rr < 64 && r0 + rr < n;
+            tok[u] = valid[u] ? __ldg(rows + r0 + rr) : 0;
+        }
+        float y[kRowsPerStep][8];
+        load_rows8<kRowsPerStep>(base, valid, tok, d, sub, pl, pos, tab, strip, y);
+#pragma unroll
+        for (int u = 0; u < kRowsPerStep; ++u) {
+            const int rr = b + u * rpi + rq;
+            if (rr < 64) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) tile[(sub * 8 + i) * 65 + rr] = valid[u] ? y[u][i] - mu[i] : 0.f;
+            }
         }
     }
     __syncthreads();

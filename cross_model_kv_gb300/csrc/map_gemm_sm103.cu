@@ -5,36 +5,61 @@
 // ("Cross-Model KV Transfer" (VeloxQuant-MLX), "The mapping"; the features are
 // the top-k selected source layers across all KV heads, "KVBridge", "What
 // ships").  The feature matrix is never materialised: each 64-wide K-block of
-// X_t is one 128-token x 64-dim box of one (layer, head) slab of the source
+// X_t is one token-block x 64-dim box of one (layer, head) slab of the source
 // cache, fetched by TMA at coordinates (e0, token0, sel*H + h).  For K the
 // source operand is the RoPE-stripped copy written by the strip pass.
 //
-// Persistent, warp-specialised kernel, one CTA per SM:
-//   warp 0      TMA producer (one lane): A box 128x64 + W box 256x64 per stage
-//   warp 1      MMA issuer (one lane): tcgen05.mma kind::f16, M=128 N=256 K=16,
-//               accumulators in TMEM, double buffered (2 x 256 columns)
-//   warps 2..5  epilogue: TMEM -> registers, + bias, target RoPE for K
-//               (pairs (e, e+64) of one head are in the same tile), round to
-//               bf16, store straight into the target cache [t][h][token][e].
+// Two persistent, warp-specialised kernels share the epilogue:
+//   map_gemm_kernel      one CTA per SM, tiles of 128 tokens x 256 outputs,
+//                        tcgen05.mma cta_group::1 (M=128 N=256 K=16);
+//   map_gemm_pair_kernel clusters of 2 CTAs on 2 SMs, tiles of 256 tokens x
+//                        256 outputs, tcgen05.mma cta_group::2 (M=256 N=256):
+//                        each CTA stages its own 128 token rows and half of
+//                        the 256 output rows of W, so a stage is 32 KB per SM
+//                        instead of 48 KB and six stages fit instead of four.
+// Roles: warp 0 TMA producer (one lane), warp 1 MMA issuer (one lane; in the
+// pair kernel only the even CTA issues), warps 2..5 epilogue: TMEM ->
+// registers, + bias, target RoPE for K (pairs (e, e+64) of one head are in the
+// same tile), round to bf16, store straight into the target cache
+// [t][h][token][e].  Accumulators are double buffered in TMEM (2 x 256 columns).
 // Every wait is bounded (DevErr::timeout_ns); on expiry the CTA records
 // DEV_ERR_TIMEOUT, stops, drains its copies and MMAs and frees TMEM.
+#include <cstdlib>
+#include <cstring>
+
 #include "kvb_internal.h"
 
 namespace kvb {
 
 namespace {
 
+constexpr int BN = 256;  // outputs per tile (two heads of 128)
+constexpr int BK = 64;   // one 128-byte swizzle atom of bf16
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr uint64_t DRAIN_NS = 200ull * 1000 * 1000;
+
+// single-CTA kernel
 constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int STAGES = 4;
+#ifndef KVB_MAP_STAGES
+#define KVB_MAP_STAGES 4
+#endif
+constexpr int STAGES = KVB_MAP_STAGES;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
-constexpr int TMEM_COLS = 512;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr uint64_t DRAIN_NS = 200ull * 1000 * 1000;
+
+// CTA-pair kernel: per CTA 128 token rows and 128 of the 256 output rows
+constexpr int PM = 256;
+#ifndef KVB_MAP_PAIR_STAGES
+#define KVB_MAP_PAIR_STAGES 6
+#endif
+constexpr int PSTAGES = KVB_MAP_PAIR_STAGES;
+constexpr int PA_BYTES = 128 * BK * 2;
+constexpr int PB_BYTES = 128 * BK * 2;
+constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
+constexpr int PSMEM_BYTES = PSTAGES * PSTAGE_BYTES + 1024 + 256;
 
 struct Params {
     int L_t, H, d, T, num_m, num_n, nk, total_tiles, max_pos;
@@ -61,6 +86,87 @@ __device__ __forceinline__ TileCoord decode_tile(const Params& P, int tile) {
     return c;
 }
 
+// K-block kb of target layer t: (source layer, head, first dim) of its box.
+__device__ __forceinline__ void kblock_source(const Params& P, int kv, int t, int kb, int q, int& layer, int& h,
+                                              int& e0) {
+    const int f0 = kb * BK;
+    const int j = f0 / q;
+    const int rem = f0 - j * q;
+    h = rem / P.d;
+    e0 = rem - h * P.d;
+    layer = P.sel.s[kv][t][j];
+}
+
+// One thread's row of one accumulator tile (256 columns = two heads): bias,
+// target RoPE for keys, bf16 rounding, store into [t][h][tok][e].
+__device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c, int tok, uint32_t tbase, int q) {
+    const bool valid = tok < P.T;
+    int p = valid ? __ldg(P.pos + tok) : 0;
+    bool bad_pos = false;
+    if (valid && (p < 0 || p >= P.max_pos)) {  // recorded; the row is written as zeros
+        dev_err_set(P.err, DEV_ERR_BAD_POS);
+        bad_pos = true;
+        p = 0;
+    }
+    const int half = P.d >> 1;  // 64
+    const int heads_per_tile = BN / P.d;
+    const float* bias = P.bias[c.kv] + static_cast<int64_t>(c.t) * q + c.n * BN;
+    const float2* tab = P.tab_t + static_cast<int64_t>(p) * half;
+    for (int hh = 0; hh < heads_per_tile; ++hh) {
+        const int h = c.n * heads_per_tile + hh;
+        __nv_bfloat16* orow = P.out[c.kv] + ((static_cast<int64_t>(c.t) * P.H + h) * P.T + tok) * P.d;
+#pragma unroll 1
+        for (int e0 = 0; e0 < half; e0 += 16) {
+            uint32_t lo[16], hi[16];
+            tmem_ld16(tbase + hh * P.d + e0, lo);
+            tmem_ld16(tbase + hh * P.d + half + e0, hi);
+            tmem_ld_wait();
+            float xl[16], xh[16];
+            const float4* bl = reinterpret_cast<const float4*>(bias + hh * P.d + e0);
+            const float4* bh = reinterpret_cast<const float4*>(bias + hh * P.d + half + e0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const float4 a = __ldg(bl + v);
+                const float4 b = __ldg(bh + v);
+                xl[4 * v + 0] = __uint_as_float(lo[4 * v + 0]) + a.x;
+                xl[4 * v + 1] = __uint_as_float(lo[4 * v + 1]) + a.y;
+                xl[4 * v + 2] = __uint_as_float(lo[4 * v + 2]) + a.z;
+                xl[4 * v + 3] = __uint_as_float(lo[4 * v + 3]) + a.w;
+                xh[4 * v + 0] = __uint_as_float(hi[4 * v + 0]) + b.x;
+                xh[4 * v + 1] = __uint_as_float(hi[4 * v + 1]) + b.y;
+                xh[4 * v + 2] = __uint_as_float(hi[4 * v + 2]) + b.z;
+                xh[4 * v + 3] = __uint_as_float(hi[4 * v + 3]) + b.w;
+            }
+            if (c.kv == 0) {
+                const float4* tp = reinterpret_cast<const float4*>(tab + e0);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const float4 cs = __ldg(tp + v);  // (c, s) of pairs 2v and 2v+1
+                    const float l0 = xl[2 * v], h0 = xh[2 * v];
+                    const float l1 = xl[2 * v + 1], h1 = xh[2 * v + 1];
+                    xl[2 * v] = fmaf(l0, cs.x, -(h0 * cs.y));
+                    xh[2 * v] = fmaf(h0, cs.x, l0 * cs.y);
+                    xl[2 * v + 1] = fmaf(l1, cs.z, -(h1 * cs.w));
+                    xh[2 * v + 1] = fmaf(h1, cs.z, l1 * cs.w);
+                }
+            }
+            if (valid) {
+                uint32_t pl[8], ph[8];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    pl[v] = bad_pos ? 0u : pack_bf16x2(xl[2 * v], xl[2 * v + 1]);
+                    ph[v] = bad_pos ? 0u : pack_bf16x2(xh[2 * v], xh[2 * v + 1]);
+                }
+                st_global_v4(orow + e0, make_uint4(pl[0], pl[1], pl[2], pl[3]));
+                st_global_v4(orow + e0 + 8, make_uint4(pl[4], pl[5], pl[6], pl[7]));
+                st_global_v4(orow + half + e0, make_uint4(ph[0], ph[1], ph[2], ph[3]));
+                st_global_v4(orow + half + e0 + 8, make_uint4(ph[4], ph[5], ph[6], ph[7]));
+            }
+        }
+    }
+}
+
+// ============================================================ single CTA
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     map_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                     const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
@@ -129,14 +235,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                    const int f0 = kb * BK;
-                    const int j = f0 / q;
-                    const int rem = f0 - j * q;
-                    const int h = rem / P.d;
-                    const int e0 = rem - h * P.d;
-                    const int layer = P.sel.s[c.kv][c.t][j];
+                    int layer, h, e0;
+                    kblock_source(P, c.kv, c.t, kb, q, layer, h, e0);
                     tma_load_3d(sA + stage * A_BYTES, ta, &full[stage], e0, c.m * BM, layer * P.H + h);
-                    tma_load_3d(sB + stage * B_BYTES, tw, &full[stage], f0, c.n * BN, c.t);
+                    tma_load_3d(sB + stage * B_BYTES, tw, &full[stage], kb * BK, c.n * BN, c.t);
                     issued_phase[stage] = static_cast<int>(phase);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -193,79 +295,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // -------------------------------------------------------- epilogue
         const int sub = warp & 3;  // TMEM lane quarter this warp may access
         const int row = sub * 32 + lane;
-        const int half = P.d >> 1;  // 64
-        const int heads_per_tile = BN / P.d;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
             const TileCoord c = decode_tile(P, tile);
             if (!mbar_wait(&tfull[acc], acc_phase, P.err, abort_flag)) break;
             tc_fence_after();
-            const int tok = c.m * BM + row;
-            const bool valid = tok < P.T;
-            int p = valid ? __ldg(P.pos + tok) : 0;
-            bool bad_pos = false;
-            if (valid && (p < 0 || p >= P.max_pos)) {  // recorded; the row is written as zeros
-                dev_err_set(P.err, DEV_ERR_BAD_POS);
-                bad_pos = true;
-                p = 0;
-            }
-            const float* bias = P.bias[c.kv] + static_cast<int64_t>(c.t) * q + c.n * BN;
-            const float2* tab = P.tab_t + static_cast<int64_t>(p) * half;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            for (int hh = 0; hh < heads_per_tile; ++hh) {
-                const int h = c.n * heads_per_tile + hh;
-                __nv_bfloat16* orow =
-                    P.out[c.kv] + ((static_cast<int64_t>(c.t) * P.H + h) * P.T + tok) * P.d;
-#pragma unroll 1
-                for (int e0 = 0; e0 < half; e0 += 16) {
-                    uint32_t lo[16], hi[16];
-                    tmem_ld16(tbase + hh * P.d + e0, lo);
-                    tmem_ld16(tbase + hh * P.d + half + e0, hi);
-                    tmem_ld_wait();
-                    float xl[16], xh[16];
-                    const float4* bl = reinterpret_cast<const float4*>(bias + hh * P.d + e0);
-                    const float4* bh = reinterpret_cast<const float4*>(bias + hh * P.d + half + e0);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const float4 a = __ldg(bl + v);
-                        const float4 b = __ldg(bh + v);
-                        xl[4 * v + 0] = __uint_as_float(lo[4 * v + 0]) + a.x;
-                        xl[4 * v + 1] = __uint_as_float(lo[4 * v + 1]) + a.y;
-                        xl[4 * v + 2] = __uint_as_float(lo[4 * v + 2]) + a.z;
-                        xl[4 * v + 3] = __uint_as_float(lo[4 * v + 3]) + a.w;
-                        xh[4 * v + 0] = __uint_as_float(hi[4 * v + 0]) + b.x;
-                        xh[4 * v + 1] = __uint_as_float(hi[4 * v + 1]) + b.y;
-                        xh[4 * v + 2] = __uint_as_float(hi[4 * v + 2]) + b.z;
-                        xh[4 * v + 3] = __uint_as_float(hi[4 * v + 3]) + b.w;
-                    }
-                    if (c.kv == 0) {
-                        const float4* tp = reinterpret_cast<const float4*>(tab + e0);
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            const float4 cs = __ldg(tp + v);  // (c, s) of pairs 2v and 2v+1
-                            const float l0 = xl[2 * v], h0 = xh[2 * v];
-                            const float l1 = xl[2 * v + 1], h1 = xh[2 * v + 1];
-                            xl[2 * v] = fmaf(l0, cs.x, -(h0 * cs.y));
-                            xh[2 * v] = fmaf(h0, cs.x, l0 * cs.y);
-                            xl[2 * v + 1] = fmaf(l1, cs.z, -(h1 * cs.w));
-                            xh[2 * v + 1] = fmaf(h1, cs.z, l1 * cs.w);
-                        }
-                    }
-                    if (valid) {
-                        uint32_t pl[8], ph[8];
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            pl[v] = bad_pos ? 0u : pack_bf16x2(xl[2 * v], xl[2 * v + 1]);
-                            ph[v] = bad_pos ? 0u : pack_bf16x2(xh[2 * v], xh[2 * v + 1]);
-                        }
-                        st_global_v4(orow + e0, make_uint4(pl[0], pl[1], pl[2], pl[3]));
-                        st_global_v4(orow + e0 + 8, make_uint4(pl[4], pl[5], pl[6], pl[7]));
-                        st_global_v4(orow + half + e0, make_uint4(ph[0], ph[1], ph[2], ph[3]));
-                        st_global_v4(orow + half + e0 + 8, make_uint4(ph[4], ph[5], ph[6], ph[7]));
-                    }
-                }
-            }
+            epilogue_row(P, c, c.m * BM + row, tbase, q);
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
             acc ^= 1;
@@ -279,6 +316,172 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ============================================================ CTA pair
+// Cluster of two CTAs (ranks 0 and 1).  Tile (kv, t, m, n) covers tokens
+// [256m, 256m + 256) and outputs [256n, 256n + 256); CTA r stages tokens
+// 256m + 128r .. +128 (A) and outputs 256n + 128r .. +128 (B) and owns the
+// accumulator rows of its tokens.  Both CTAs' copies complete on rank 0's
+// `full` barrier; rank 0 issues the pair MMAs and commits to both CTAs'
+// `empty` / `tfull` barriers; both CTAs' epilogues arrive on rank 0's `tempty`.
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    map_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                         const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+                         const __grid_constant__ Params P) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + PSTAGES * PA_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + PSTAGES * PSTAGE_BYTES);
+    uint64_t* empty = full + PSTAGES;
+    uint64_t* tfull = empty + PSTAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PSTAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 2 * 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a0);
+        tma_prefetch_desc(&tm_a1);
+        tma_prefetch_desc(&tm_w0);
+        tma_prefetch_desc(&tm_w1);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();  // both CTAs' barriers are initialised before any remote signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int q = P.H * P.d;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------------- producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_phase[PSTAGES];
+            for (int s = 0; s < PSTAGES; ++s) issued_phase[s] = -1;
+            bool ok = true;
+            for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
+                const TileCoord c = decode_tile(P, tile);
+                const CUtensorMap* ta = c.kv ? &tm_a1 : &tm_a0;
+                const CUtensorMap* tw = c.kv ? &tm_w1 : &tm_w0;
+                for (int kb = 0; kb < P.nk; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * PSTAGE_BYTES);
+                    int layer, h, e0;
+                    kblock_source(P, c.kv, c.t, kb, q, layer, h, e0);
+                    tma_load_3d_pair(sA + stage * PA_BYTES, ta, full_leader, e0, c.m * PM + 128 * rank,
+                                     layer * P.H + h);
+                    tma_load_3d_pair(sB + stage * PB_BYTES, tw, full_leader, kb * BK, c.n * BN + 128 * rank, c.t);
+                    issued_phase[stage] = static_cast<int>(phase);
+                    if (++stage == PSTAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // The leader's full barriers count both CTAs' bytes: drain there.
+            if (leader)
+                for (int s = 0; s < PSTAGES; ++s)
+                    if (issued_phase[s] >= 0)
+                        mbar_wait_drain(&full[s], static_cast<uint32_t>(issued_phase[s]), DRAIN_NS);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------------------------------------------- MMA issuer (rank 0)
+            constexpr uint32_t idesc = idesc_bf16_f32(PM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, P.err, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < P.nk; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, P.err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + stage * PA_BYTES);
+                    const uint32_t b0 = smem_u32(sB + stage * PB_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        umma_bf16_pair(d_tmem, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc,
+                                       (kb | k) != 0);
+                    }
+                    umma_commit_pair(&empty[stage], 0x3);
+                    if (++stage == PSTAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(&tfull[acc], 0x3);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            umma_commit_pair(drain, 0x1);
+            mbar_wait_drain(drain, 0, DRAIN_NS);
+        }
+    } else {
+        // -------------------------------------------------------- epilogue (both CTAs)
+        const int sub = warp & 3;
+        const int row = sub * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = pair; tile < P.total_tiles; tile += npairs) {
+            const TileCoord c = decode_tile(P, tile);
+            if (!mbar_wait(&tfull[acc], acc_phase, P.err, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            epilogue_row(P, c, c.m * PM + 128 * static_cast<int>(rank) + row, tbase, q);
+            tc_fence_before();
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync_all();  // no CTA leaves while its pair may still read its shared memory or TMEM
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -303,6 +506,11 @@ bool encode_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, 
     return true;
 }
 
+bool use_pair_kernel() {
+    const char* s = std::getenv("KVB_MAP_PAIR");
+    return s && std::strcmp(s, "1") == 0;
+}
+
 }  // namespace
 
 bool map_gemm_tc_supported(const Shape& sh) {
@@ -314,12 +522,14 @@ cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string
     const Shape& sh = a.sh;
     const int q = sh.H * sh.d;
     const int p = sh.k * q;
+    const bool pair = use_pair_kernel() && a.num_sms >= 2;
+    const int tm = pair ? PM : BM;
     Params P{};
     P.L_t = sh.L_t;
     P.H = sh.H;
     P.d = sh.d;
     P.T = static_cast<int>(sh.T);
-    P.num_m = static_cast<int>((sh.T + BM - 1) / BM);
+    P.num_m = static_cast<int>((sh.T + tm - 1) / tm);
     P.num_n = q / BN;
     P.nk = p / BK;
     const int64_t total = 2LL * sh.L_t * P.num_m * P.num_n;
@@ -339,14 +549,35 @@ cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string
     }
     CUtensorMap tma[2], tmw[2];
     for (int kv = 0; kv < 2; ++kv) {
-        if (!encode_3d_bf16(&tma[kv], a.a_src[kv], sh.d, sh.T, static_cast<uint64_t>(sh.L_s) * sh.H, BK, BM, why))
+        if (!encode_3d_bf16(&tma[kv], a.a_src[kv], sh.d, sh.T, static_cast<uint64_t>(sh.L_s) * sh.H, BK, 128, why))
             return cudaErrorInvalidValue;
-        if (!encode_3d_bf16(&tmw[kv], a.w[kv], p, q, sh.L_t, BK, BN, why)) return cudaErrorInvalidValue;
+        if (!encode_3d_bf16(&tmw[kv], a.w[kv], p, q, sh.L_t, BK, pair ? 128 : BN, why)) return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(map_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (!pair) {
+        cudaError_t e = cudaFuncSetAttribute(map_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        const int grid = static_cast<int>(total < a.num_sms ? total : a.num_sms);
+        map_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tma[0], tma[1], tmw[0], tmw[1], P);
+        return cudaGetLastError();
+    }
+    cudaError_t e = cudaFuncSetAttribute(map_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PSMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int grid = static_cast<int>(total < a.num_sms ? total : a.num_sms);
-    map_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tma[0], tma[1], tmw[0], tmw[1], P);
+    int pairs = a.num_sms / 2;
+    if (total < pairs) pairs = static_cast<int>(total);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = PSMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, map_gemm_pair_kernel, tma[0], tma[1], tmw[0], tmw[1], P);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -1,11 +1,17 @@
-// Calibration statistics: stride gather, RoPE strip, batch means, centering,
-// Chan merge coefficients, and the CUDA-core statistics GEMM.
+// Calibration statistics: stride gather, RoPE strip, shifted centering, Chan
+// merge coefficients, and the CUDA-core statistics GEMM.
 //
 // "KVBridge" README, "Loading": only centered sufficient statistics are kept,
-// merged batch by batch with Chan/Welford updates:
-//   n = n_a + n_b,  delta = mean_b - mean_a,  f = n_a n_b / n,
-//   M <- M + M_b + f delta_x delta_x^T,  C <- C + C_b + f delta_x delta_y^T,
-//   S_yy <- S_yy + S_yy,b + f delta_y^2,  mean <- mean_a + delta n_b / n.
+// merged batch by batch with Chan/Welford updates.  With a per-column shift s
+// (any value known before the pass) and z = x - s over the n_b kept rows of a
+// batch, zbar = mean(z), the batch mean is s + zbar and
+//   n = n_a + n_b,  delta = (s + zbar) - mean_a,  f = n_a n_b / n,
+//   M <- M + Z^T Z - n_b zbar zbar^T + f delta delta^T        (same for C, S_yy)
+//   mean <- mean_a + delta n_b / n.
+// Z^T Z - n_b zbar zbar^T is the batch's centered Gram exactly; with s near the
+// batch mean (the running mean, or the batch's first kept row for the first
+// batch) the subtraction is tiny, so no cancellation from large raw moments.
+// The generic path centers on the batch mean itself (s = batch mean, zbar = 0).
 // "Cross-Model KV Transfer" (VeloxQuant-MLX), "Configuration": deterministic
 // token stride 4 (positions that are multiples of the stride are kept).
 // Keys are stripped of RoPE with their own model's theta before any statistic.
@@ -70,6 +76,11 @@ __global__ void __launch_bounds__(1024) select_rows_kernel(const int* __restrict
     if (threadIdx.x == 0) *nb = base;
 }
 
+// ---------------------------------------------------------------------------
+// Generic path (any even head_dim, fp32 or bf16 caches): two passes, the
+// batch means first, then centering on them.
+// ---------------------------------------------------------------------------
+
 // Value of feature column e of one stored row, RoPE-stripped for keys.
 template <typename T>
 __device__ __forceinline__ float feature_value(const T* row, int e, int half, bool strip, const float2* tab_row) {
@@ -112,11 +123,11 @@ __global__ void __launch_bounds__(256) colmean_kernel(const T* __restrict__ cach
     }
 }
 
-// Centered, transposed compaction: v = value(row r, f) - batch mean[f] for
-// r < n_b, zero for n_b <= r < round_up(n_b, 64), stored at [f][r].  With
-// out_lo == nullptr v is stored as float32; otherwise as the bf16 pair
-// hi = bf16(v), lo = bf16(v - hi) (hi + lo carries ~16 significant bits), the
-// operand form of the tensor-core statistics GEMM.  Grid (slab, 64-row chunk).
+// Centered, transposed compaction: z = value(row r, f) - mean[f] for r < n_b,
+// zero for n_b <= r < round_up(n_b, 64), stored at [f][r].  With out_lo ==
+// nullptr z is stored as float32; otherwise as the bf16 pair hi = bf16(z),
+// lo = bf16(z - hi) (hi + lo carries ~16 significant bits), the operand form
+// of the tensor-core statistics GEMM.  Grid (slab, 64-row chunk).
 template <typename T>
 __global__ void __launch_bounds__(256) center_transpose_kernel(const T* __restrict__ cache, int64_t T_len, int d,
                                                                const int* __restrict__ rows,
@@ -166,12 +177,11 @@ __global__ void __launch_bounds__(256) center_transpose_kernel(const T* __restri
 }
 
 // ---------------------------------------------------------------------------
-// Vectorised gather for bf16 caches with head_dim % 16 == 0: each lane owns 8
-// contiguous dims of a row (one 16-byte load); the RoPE partner dims of the
-// same row sit in lane ^ (d/16), fetched with a shuffle.  Each thread handles
-// R rows per step with all their loads issued before any use, so R row loads,
-// position loads and table loads are in flight at once.  Loops are
-// warp-uniform so the shuffles always see the whole warp.
+// Single-pass path for bf16 caches with head_dim % 16 == 0.  Each lane owns 8
+// RoPE pairs of a row: 8 dims of the low half and the 8 partner dims of the
+// high half (two 16-byte loads, one 64-byte cos/sin load), the layout of the
+// strip pass.  The shift s is known before the pass: the running mean, or for
+// the first batch the first kept row of the batch.  One read of every kept row.
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
@@ -184,193 +194,213 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
     }
 }
 
-// Stripped (keys) or raw (values) features of 8 dims of R kept rows.
-template <int R>
-__device__ __forceinline__ void load_rows8(const __nv_bfloat16* __restrict__ slab_base, const bool (&valid)[R],
-                                           const int (&tok)[R], int d, int sub, int pl,
-                                           const int* __restrict__ pos, const float2* __restrict__ tab, bool strip,
-                                           float (&y)[R][8]) {
-    uint4 raw[R];
-#pragma unroll
-    for (int u = 0; u < R; ++u)
-        raw[u] = valid[u] ? __ldg(reinterpret_cast<const uint4*>(slab_base + static_cast<int64_t>(tok[u]) * d + sub * 8))
-                          : make_uint4(0, 0, 0, 0);
+// Stripped (keys) or raw (values) dims [8l, 8l+8) and [half+8l, half+8l+8) of one row.
+__device__ __forceinline__ void pair8(const __nv_bfloat16* __restrict__ row, int l, int half, bool strip,
+                                      const float2* __restrict__ tab_row, float (&lo)[8], float (&hi)[8]) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(row + 8 * l));
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(row + half + 8 * l));
+    float x[8], y[8];
+    unpack8(a, x);
+    unpack8(b, y);
     if (!strip) {
 #pragma unroll
-        for (int u = 0; u < R; ++u) unpack8(raw[u], y[u]);
+        for (int i = 0; i < 8; ++i) {
+            lo[i] = x[i];
+            hi[i] = y[i];
+        }
         return;
     }
-    const int half = d >> 1;
-    const bool lo = sub < pl;
-    const int i0 = lo ? sub * 8 : sub * 8 - half;
-    float4 cs[R][4];
+    const float4* t4 = reinterpret_cast<const float4*>(tab_row + 8 * l);
 #pragma unroll
-    for (int u = 0; u < R; ++u) {
-        const int p = valid[u] ? __ldg(pos + tok[u]) : 0;
-        const float4* t4 = reinterpret_cast<const float4*>(tab + static_cast<int64_t>(p) * half + i0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) cs[u][q] = __ldg(t4 + q);
-    }
-#pragma unroll
-    for (int u = 0; u < R; ++u) {
-        uint4 pr;
-        pr.x = __shfl_xor_sync(0xffffffffu, raw[u].x, pl);
-        pr.y = __shfl_xor_sync(0xffffffffu, raw[u].y, pl);
-        pr.z = __shfl_xor_sync(0xffffffffu, raw[u].z, pl);
-        pr.w = __shfl_xor_sync(0xffffffffu, raw[u].w, pl);
-        float x[8], p[8];
-        unpack8(raw[u], x);
-        unpack8(pr, p);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {  // cs = (c, s) of two consecutive pairs
-            const float s0 = lo ? cs[u][q].y : -cs[u][q].y, s1 = lo ? cs[u][q].w : -cs[u][q].w;
-            y[u][2 * q] = fmaf(x[2 * q], cs[u][q].x, p[2 * q] * s0);
-            y[u][2 * q + 1] = fmaf(x[2 * q + 1], cs[u][q].z, p[2 * q + 1] * s1);
-        }
+    for (int q = 0; q < 4; ++q) {
+        const float4 cs = __ldg(t4 + q);  // (c, s) of pairs 2q and 2q+1
+        lo[2 * q] = fmaf(x[2 * q], cs.x, y[2 * q] * cs.y);
+        hi[2 * q] = fmaf(y[2 * q], cs.x, -(x[2 * q] * cs.y));
+        lo[2 * q + 1] = fmaf(x[2 * q + 1], cs.z, y[2 * q + 1] * cs.w);
+        hi[2 * q + 1] = fmaf(y[2 * q + 1], cs.z, -(x[2 * q + 1] * cs.w));
     }
 }
 
-constexpr int kRowsPerStep = 4;
+constexpr int kChunk = 128;  // kept rows per CTA of the single-pass gather
 
-// Partial column sums: part[split][slab*d + e] over the split's share of kept rows.
-__global__ void __launch_bounds__(256) colsum_vec_kernel(const __nv_bfloat16* __restrict__ cache, int64_t T_len,
-                                                         int d, const int* __restrict__ rows,
-                                                         const int* __restrict__ nb, const int* __restrict__ pos,
-                                                         const float2* __restrict__ tab, bool strip,
-                                                         float* __restrict__ part, int64_t F) {
-    __shared__ float red[256 * 8];
-    const int slab = blockIdx.x, split = blockIdx.y, S = gridDim.y;
-    const int lpr = d >> 3;           // lanes per row
-    const int rpi = 256 / lpr;        // rows per row-slot sweep
-    const int sub = threadIdx.x % lpr;
-    const int rr = threadIdx.x / lpr;
-    const int pl = d >> 4;
+// Grid (slab, 128-row chunk), 256 threads; each thread owns R rows of its lane
+// column (R = 128 / rows-per-sweep) and issues all their loads before any use.
+// Writes z = feature - s transposed ([f][r], float32 or bf16 hi/lo), the
+// chunk's column sums of z to part[chunk][slab*d + e], and (chunk 0) the shift.
+template <int R>
+__global__ void __launch_bounds__(256, (R <= 4 ? 2 : 1)) gather_shift_kernel(const __nv_bfloat16* __restrict__ cache, int64_t T_len,
+                                                           int d, const int* __restrict__ rows,
+                                                           const int* __restrict__ nb,
+                                                           const long long* __restrict__ n_seen,
+                                                           const int* __restrict__ pos,
+                                                           const float2* __restrict__ tab, bool strip,
+                                                           const float* __restrict__ mean_a,
+                                                           float* __restrict__ shift_out, float* __restrict__ part,
+                                                           int64_t F, void* __restrict__ out,
+                                                           void* __restrict__ out_lo, int64_t ld) {
+    extern __shared__ float tile[];  // [d][kChunk + 1] then [rps][d] partial sums
+    constexpr int LT = kChunk + 1;
+    const int slab = blockIdx.x;
+    const int chunk = blockIdx.y;
+    const int r0 = chunk * kChunk;
     const int n = *nb;
-    const int chunk = (n + S - 1) / S;
-    const int r0 = split * chunk, r1 = min(n, r0 + chunk);
+    if (r0 >= ((n + kChunk - 1) / kChunk) * kChunk) return;
+    const int half = d >> 1;
+    const int lpr = d >> 4;          // lanes per row (8 pairs each)
+    const int rps = 256 / lpr;       // rows per sweep
+    const int l = threadIdx.x % lpr;
+    const int rq = threadIdx.x / lpr;
     const __nv_bfloat16* base = cache + static_cast<int64_t>(slab) * T_len * d;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int b = r0; b < r1; b += rpi * kRowsPerStep) {
-        bool valid[kRowsPerStep];
-        int tok[kRowsPerStep];
+    const int64_t f0 = static_cast<int64_t>(slab) * d;
+
+    // issue every load of this thread's rows first
+    uint4 ra[R], rb[R];
+    float4 cs[R][4];
+    bool valid[R];
 #pragma unroll
-        for (int u = 0; u < kRowsPerStep; ++u) {
-            const int r = b + u * rpi + rr;
-            valid[u] = r < r1;
-            tok[u] = valid[u] ? __ldg(rows + r) : 0;
+    for (int u = 0; u < R; ++u) {
+        const int rr = rq + u * rps;
+        const int r = r0 + rr;
+        valid[u] = rr < kChunk && r < n;
+        const int tok = valid[u] ? __ldg(rows + r) : 0;
+        const __nv_bfloat16* row = base + static_cast<int64_t>(tok) * d;
+        ra[u] = valid[u] ? __ldg(reinterpret_cast<const uint4*>(row + 8 * l)) : make_uint4(0, 0, 0, 0);
+        rb[u] = valid[u] ? __ldg(reinterpret_cast<const uint4*>(row + half + 8 * l)) : make_uint4(0, 0, 0, 0);
+        if (strip) {
+            const int p = valid[u] ? __ldg(pos + tok) : 0;
+            const float4* t4 = reinterpret_cast<const float4*>(tab + static_cast<int64_t>(p) * half + 8 * l);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) cs[u][q] = __ldg(t4 + q);
         }
-        float y[kRowsPerStep][8];
-        load_rows8<kRowsPerStep>(base, valid, tok, d, sub, pl, pos, tab, strip, y);
-#pragma unroll
-        for (int u = 0; u < kRowsPerStep; ++u)
-            if (valid[u]) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] += y[u][i];
-            }
     }
+
+    float slo[8], shi[8];
+    if (*n_seen > 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) red[rr * d + sub * 8 + i] = acc[i];
+        for (int i = 0; i < 8; ++i) {
+            slo[i] = mean_a[f0 + 8 * l + i];
+            shi[i] = mean_a[f0 + half + 8 * l + i];
+        }
+    } else {  // first batch: shift by the first kept row (n >= 1 here)
+        const int tok = __ldg(rows);
+        pair8(base + static_cast<int64_t>(tok) * d, l, half, strip, tab + static_cast<int64_t>(__ldg(pos + tok)) * half,
+              slo, shi);
+    }
+    if (chunk == 0 && rq == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            shift_out[f0 + 8 * l + i] = slo[i];
+            shift_out[f0 + half + 8 * l + i] = shi[i];
+        }
+    }
+    float alo[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, ahi[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+        const int rr = rq + u * rps;
+        if (rr >= kChunk) continue;
+        float x[8], y[8], zl[8], zh[8];
+        unpack8(ra[u], x);
+        unpack8(rb[u], y);
+        if (strip) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                zl[2 * q] = fmaf(x[2 * q], cs[u][q].x, y[2 * q] * cs[u][q].y);
+                zh[2 * q] = fmaf(y[2 * q], cs[u][q].x, -(x[2 * q] * cs[u][q].y));
+                zl[2 * q + 1] = fmaf(x[2 * q + 1], cs[u][q].z, y[2 * q + 1] * cs[u][q].w);
+                zh[2 * q + 1] = fmaf(y[2 * q + 1], cs[u][q].z, -(x[2 * q + 1] * cs[u][q].w));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                zl[i] = x[i];
+                zh[i] = y[i];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            zl[i] = valid[u] ? zl[i] - slo[i] : 0.f;
+            zh[i] = valid[u] ? zh[i] - shi[i] : 0.f;
+            alo[i] += zl[i];
+            ahi[i] += zh[i];
+            tile[(8 * l + i) * LT + rr] = zl[i];
+            tile[(half + 8 * l + i) * LT + rr] = zh[i];
+        }
+    }
+    float* red = tile + d * LT;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        red[rq * d + 8 * l + i] = alo[i];
+        red[rq * d + half + 8 * l + i] = ahi[i];
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < d; e += blockDim.x) {
         float s = 0.f;
-        for (int q = 0; q < rpi; ++q) s += red[q * d + e];
-        part[static_cast<int64_t>(split) * F + static_cast<int64_t>(slab) * d + e] = s;
+        for (int q = 0; q < rps; ++q) s += red[q * d + e];
+        part[static_cast<int64_t>(chunk) * F + f0 + e] = s;
     }
-}
-
-__global__ void mean_finalize_kernel(const float* __restrict__ part, int S, int64_t F, const int* __restrict__ nb,
-                                     float* __restrict__ mean) {
-    const int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    if (c >= F) return;
-    const int n = *nb;
-    float s = 0.f;
-    for (int q = 0; q < S; ++q) s += part[q * F + c];
-    mean[c] = n > 0 ? s / static_cast<float>(n) : 0.f;
-}
-
-// Centered, transposed compaction of 64 kept rows of one slab (see
-// center_transpose_kernel), vectorised.  tile[e][r] in shared memory.
-__global__ void __launch_bounds__(256) center_vec_kernel(const __nv_bfloat16* __restrict__ cache, int64_t T_len,
-                                                         int d, const int* __restrict__ rows,
-                                                         const int* __restrict__ nb, const int* __restrict__ pos,
-                                                         const float2* __restrict__ tab, bool strip,
-                                                         const float* __restrict__ mean, void* __restrict__ out,
-                                                         void* __restrict__ out_lo, int64_t ld) {
-    extern __shared__ float tile[];  // [d][65]
-    const int slab = blockIdx.x;
-    const int r0 = blockIdx.y * 64;
-    const int n = *nb;
-    if (r0 >= ((n + 63) & ~63)) return;
-    const int lpr = d >> 3, rpi = 256 / lpr;
-    const int sub = threadIdx.x % lpr, rq = threadIdx.x / lpr;
-    const int pl = d >> 4;
-    const __nv_bfloat16* base = cache + static_cast<int64_t>(slab) * T_len * d;
-    float mu[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mu[i] = mean[static_cast<int64_t>(slab) * d + sub * 8 + i];
-    for (int b = 0; b < 64; b += rpi * kRowsPerStep) {
-        bool valid[kRowsPerStep];
-        int tok[kRowsPerStep];
-#pragma unroll
-        for (int u = 0; u < kRowsPerStep; ++u) {
-            const int rr = b + u * rpi + rq;
-            valid[u] = rr < 64 && r0 + rr < n;
-            tok[u] = valid[u] ? __ldg(rows + r0 + rr) : 0;
-        }
-        float y[kRowsPerStep][8];
-        load_rows8<kRowsPerStep>(base, valid, tok, d, sub, pl, pos, tab, strip, y);
-#pragma unroll
-        for (int u = 0; u < kRowsPerStep; ++u) {
-            const int rr = b + u * rpi + rq;
-            if (rr < 64) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) tile[(sub * 8 + i) * 65 + rr] = valid[u] ? y[u][i] - mu[i] : 0.f;
-            }
-        }
-    }
-    __syncthreads();
-    const int64_t row0 = static_cast<int64_t>(slab) * d;
     if (out_lo == nullptr) {
-        for (int idx = threadIdx.x; idx < d * 16; idx += blockDim.x) {
-            const int e = idx >> 4, q = idx & 15;
-            const float* t = tile + e * 65 + 4 * q;
-            *reinterpret_cast<float4*>(static_cast<float*>(out) + (row0 + e) * ld + r0 + 4 * q) =
+        for (int idx = threadIdx.x; idx < d * (kChunk / 4); idx += blockDim.x) {
+            const int e = idx / (kChunk / 4), q = idx % (kChunk / 4);
+            const float* t = tile + e * LT + 4 * q;
+            *reinterpret_cast<float4*>(static_cast<float*>(out) + (f0 + e) * ld + r0 + 4 * q) =
                 make_float4(t[0], t[1], t[2], t[3]);
         }
     } else {
-        for (int idx = threadIdx.x; idx < d * 8; idx += blockDim.x) {
-            const int e = idx >> 3, q = idx & 7;
-            const float* t = tile + e * 65 + 8 * q;
-            uint32_t hi[4], lo[4];
+        for (int idx = threadIdx.x; idx < d * (kChunk / 8); idx += blockDim.x) {
+            const int e = idx / (kChunk / 8), q = idx % (kChunk / 8);
+            const float* t = tile + e * LT + 8 * q;
+            uint32_t h[4], lw[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const __nv_bfloat16 h0 = __float2bfloat16_rn(t[2 * j]), h1 = __float2bfloat16_rn(t[2 * j + 1]);
                 const float l0 = t[2 * j] - __bfloat162float(h0), l1 = t[2 * j + 1] - __bfloat162float(h1);
                 __nv_bfloat162 hh(h0, h1);
-                hi[j] = *reinterpret_cast<uint32_t*>(&hh);
-                lo[j] = pack_bf16x2(l0, l1);
+                h[j] = *reinterpret_cast<uint32_t*>(&hh);
+                lw[j] = pack_bf16x2(l0, l1);
             }
-            const int64_t o = (row0 + e) * ld + r0 + 8 * q;
-            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_lo) + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            const int64_t o = (f0 + e) * ld + r0 + 8 * q;
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + o) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_lo) + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
     }
 }
 
-// delta = batch mean - running mean (before the merge); running mean updated;
-// f = n_a n_b / (n_a + n_b).  Thread per column over the four mean vectors.
+// zsum[c] = sum over the batch's chunks of part[chunk][c].
+__global__ void zsum_kernel(const float* __restrict__ part, int64_t F, const int* __restrict__ nb,
+                            float* __restrict__ zsum) {
+    const int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (c >= F) return;
+    const int chunks = (*nb + kChunk - 1) / kChunk;
+    float s = 0.f;
+    for (int q = 0; q < chunks; ++q) s += part[q * F + c];
+    zsum[c] = s;
+}
+
+// Per column of the four matrices: zbar, delta against the running mean, the
+// running-mean update; coef = {f = n_a n_b / n, g = n_b}.
 __global__ void chan_prepare_kernel(MeanSet ms, const long long* __restrict__ n_dev, const int* __restrict__ nb,
-                                    float* __restrict__ f_out) {
+                                    float* __restrict__ coef) {
     const long long na = *n_dev;
     const int n_b = *nb;
     const double n = static_cast<double>(na) + n_b;
     const float wb = n > 0 ? static_cast<float>(n_b / n) : 0.f;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *f_out = n > 0 ? static_cast<float>(static_cast<double>(na) * n_b / n) : 0.f;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        coef[0] = n > 0 ? static_cast<float>(static_cast<double>(na) * n_b / n) : 0.f;
+        coef[1] = static_cast<float>(n_b);
+    }
     for (int m = 0; m < 4; ++m) {
         for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < ms.len[m];
              c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-            const float dl = n_b > 0 ? ms.bmean[m][c] - ms.mean[m][c] : 0.f;
+            float zbar = 0.f, xb;
+            if (ms.zsum[m]) {
+                zbar = n_b > 0 ? ms.zsum[m][c] / static_cast<float>(n_b) : 0.f;
+                xb = ms.shift[m][c] + zbar;
+            } else {
+                xb = ms.bmean[m][c];
+            }
+            const float dl = n_b > 0 ? xb - ms.mean[m][c] : 0.f;
             ms.delta[m][c] = dl;
+            ms.zbar[m][c] = zbar;
             ms.mean[m][c] += dl * wb;
         }
     }
@@ -380,11 +410,11 @@ __global__ void chan_finish_kernel(long long* __restrict__ n_dev, const int* __r
     *n_dev += *nb;
 }
 
-// S_yy[j] += sum_r Y[j][r]^2 + f delta_y[j]^2.  One warp per target column.
-// Y is float32, or a (hi, lo) bf16 pair when lo != nullptr.
+// S_yy[j] += sum_r Z[j][r]^2 - g zbar_j^2 + f delta_j^2.  One warp per column.
+// Z is float32, or a (hi, lo) bf16 pair when lo != nullptr.
 __global__ void syy_kernel(const void* __restrict__ Y, const void* __restrict__ Ylo, int64_t ld, int64_t rows_n,
-                           const int* __restrict__ nb, const float* __restrict__ dy, const float* __restrict__ f,
-                           float* __restrict__ syy) {
+                           const int* __restrict__ nb, const float* __restrict__ dy, const float* __restrict__ zy,
+                           const float* __restrict__ coef, float* __restrict__ syy) {
     const int64_t j = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (j >= rows_n) return;
@@ -401,17 +431,19 @@ __global__ void syy_kernel(const void* __restrict__ Y, const void* __restrict__ 
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) syy[j] += s + (*f) * dy[j] * dy[j];
+    if (lane == 0) syy[j] += s - coef[1] * zy[j] * zy[j] + coef[0] * dy[j] * dy[j];
 }
 
-// out[i][j] += sum_r A[i][r] B[j][r] + f da[i] db[j] over K = round_up(n_b, 64)
-// (padding columns are zero).  64x64 tile, 256 threads, 4x4 per thread.
-// With lower != 0, tiles entirely above the diagonal are skipped.
+// out[i][j] += sum_r A[i][r] B[j][r] - g za_i zb_j + f da_i db_j over
+// K = round_up(n_b, 64) (padding columns are zero).  64x64 tiles, 256 threads,
+// 4x4 per thread.  With lower != 0, tiles entirely above the diagonal are skipped.
 __global__ void __launch_bounds__(256) stats_gemm_simt_kernel(const float* __restrict__ A, const float* __restrict__ B,
                                                               int64_t ld, int64_t Ma, int64_t Nb, int lower,
                                                               const float* __restrict__ da,
                                                               const float* __restrict__ db,
-                                                              const float* __restrict__ f,
+                                                              const float* __restrict__ za,
+                                                              const float* __restrict__ zb,
+                                                              const float* __restrict__ coef,
                                                               const int* __restrict__ nb, float* __restrict__ out,
                                                               int64_t ldo) {
     constexpr int BT = 64, BKK = 16;
@@ -444,17 +476,17 @@ __global__ void __launch_bounds__(256) stats_gemm_simt_kernel(const float* __res
         }
         __syncthreads();
     }
-    const float ff = *f;
+    const float ff = coef[0], gg = coef[1];
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
         const int64_t i = i0 + ty * 4 + x;
         if (i >= Ma) continue;
-        const float fa = ff * da[i];
+        const float fa = ff * da[i], ga = gg * za[i];
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
             const int64_t j = j0 + tx * 4 + y;
             if (j >= Nb) continue;
-            out[i * ldo + j] += acc[x][y] + fa * db[j];
+            out[i * ldo + j] += acc[x][y] - ga * zb[j] + fa * db[j];
         }
     }
 }
@@ -483,59 +515,63 @@ cudaError_t launch_select_rows(const int* pos, int64_t T, int stride, int max_po
     return cudaGetLastError();
 }
 
-constexpr int kMeanSplits = 8;
+bool gather_single_pass_ok(kvb_dtype dt, int d) { return dt == KVB_BF16 && d % 16 == 0 && d <= 256; }
 
-bool gather_vec_ok(kvb_dtype dt, int d) { return dt == KVB_BF16 && d % 16 == 0 && d <= 256; }
-
-cudaError_t launch_colmean(kvb_dtype dt, const void* cache, int64_t n_slabs, int64_t T, int d, const int* rows,
-                           const int* nb, const int* pos, const float2* tab, bool strip, float* mean, float* part,
-                           cudaStream_t s) {
-    if (n_slabs == 0) return cudaSuccess;
-    if (gather_vec_ok(dt, d) && part != nullptr) {
-        const int64_t F = n_slabs * d;
-        colsum_vec_kernel<<<dim3(static_cast<unsigned>(n_slabs), kMeanSplits), 256, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(cache), T, d, rows, nb, pos, tab, strip, part, F);
-        mean_finalize_kernel<<<static_cast<unsigned>((F + 255) / 256), 256, 0, s>>>(part, kMeanSplits, F, nb, mean);
-    } else if (dt == KVB_F32) {
-        colmean_kernel<float><<<static_cast<unsigned>(n_slabs), 256, 0, s>>>(
-            static_cast<const float*>(cache), T, d, rows, nb, pos, tab, strip, mean);
-    } else {
-        colmean_kernel<__nv_bfloat16><<<static_cast<unsigned>(n_slabs), 256, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(cache), T, d, rows, nb, pos, tab, strip, mean);
-    }
-    return cudaGetLastError();
-}
-
-cudaError_t launch_center_transpose(kvb_dtype dt, const void* cache, int64_t n_slabs, int64_t T, int d,
-                                    const int* rows, const int* nb, const int* pos, const float2* tab, bool strip,
-                                    const float* mean, void* out, void* out_lo, int64_t ld, cudaStream_t s) {
-    if (n_slabs == 0) return cudaSuccess;
-    dim3 grid(static_cast<unsigned>(n_slabs), static_cast<unsigned>((T + 63) / 64));
-    if (gather_vec_ok(dt, d)) {
-        const size_t vsmem = static_cast<size_t>(d) * 65 * sizeof(float);
-        cudaFuncSetAttribute(center_vec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 80 * 1024);
-        center_vec_kernel<<<grid, 256, vsmem, s>>>(static_cast<const __nv_bfloat16*>(cache), T, d, rows, nb, pos, tab,
-                                                   strip, mean, out, out_lo, ld);
+cudaError_t launch_gather(const GatherArgs& g, cudaStream_t s) {
+    if (g.n_slabs == 0) return cudaSuccess;
+    const int64_t F = g.n_slabs * g.d;
+    dim3 grid(static_cast<unsigned>(g.n_slabs), static_cast<unsigned>((g.T + 63) / 64));
+    if (gather_single_pass_ok(g.dt, g.d)) {
+        const int rps = 256 / (g.d >> 4);
+        const int R = rps >= kChunk ? 1 : kChunk / rps;
+        const size_t smem = (static_cast<size_t>(g.d) * (kChunk + 1) + static_cast<size_t>(rps) * g.d) * sizeof(float);
+        dim3 cgrid(static_cast<unsigned>(g.n_slabs), static_cast<unsigned>((g.T + kChunk - 1) / kChunk));
+        const __nv_bfloat16* c16 = static_cast<const __nv_bfloat16*>(g.cache);
+#define KVB_GATHER(RR)                                                                                          \
+    do {                                                                                                        \
+        cudaError_t e = cudaFuncSetAttribute(gather_shift_kernel<RR>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                             200 * 1024);                                                       \
+        if (e != cudaSuccess) return e;                                                                         \
+        gather_shift_kernel<RR><<<cgrid, 256, smem, s>>>(c16, g.T, g.d, g.rows, g.nb, g.n_seen, g.pos, g.tab,   \
+                                                         g.strip, g.mean_a, g.shift, g.part, F, g.out, g.out_lo, \
+                                                         g.ld);                                                 \
+    } while (0)
+        switch (R) {
+            case 1: KVB_GATHER(1); break;
+            case 2: KVB_GATHER(2); break;
+            case 4: KVB_GATHER(4); break;
+            default: KVB_GATHER(8); break;
+        }
+#undef KVB_GATHER
+        zsum_kernel<<<static_cast<unsigned>((F + 255) / 256), 256, 0, s>>>(g.part, F, g.nb, g.zsum);
         return cudaGetLastError();
     }
-    const size_t smem = 64 * (d + 1) * sizeof(float);
-    if (dt == KVB_F32) {
+    // generic two-pass path: batch means, then centering on them (zbar = 0)
+    if (g.dt == KVB_F32)
+        colmean_kernel<float><<<static_cast<unsigned>(g.n_slabs), 256, 0, s>>>(
+            static_cast<const float*>(g.cache), g.T, g.d, g.rows, g.nb, g.pos, g.tab, g.strip, g.bmean);
+    else
+        colmean_kernel<__nv_bfloat16><<<static_cast<unsigned>(g.n_slabs), 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(g.cache), g.T, g.d, g.rows, g.nb, g.pos, g.tab, g.strip, g.bmean);
+    const size_t smem = 64 * (g.d + 1) * sizeof(float);
+    if (g.dt == KVB_F32) {
         cudaFuncSetAttribute(center_transpose_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 80 * 1024);
-        center_transpose_kernel<float><<<grid, 256, smem, s>>>(static_cast<const float*>(cache), T, d, rows, nb, pos,
-                                                               tab, strip, mean, out, out_lo, ld);
+        center_transpose_kernel<float><<<grid, 256, smem, s>>>(static_cast<const float*>(g.cache), g.T, g.d, g.rows,
+                                                               g.nb, g.pos, g.tab, g.strip, g.bmean, g.out, g.out_lo,
+                                                               g.ld);
     } else {
         cudaFuncSetAttribute(center_transpose_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              80 * 1024);
-        center_transpose_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(cache), T, d,
-                                                                       rows, nb, pos, tab, strip, mean, out, out_lo,
-                                                                       ld);
+        center_transpose_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(
+            static_cast<const __nv_bfloat16*>(g.cache), g.T, g.d, g.rows, g.nb, g.pos, g.tab, g.strip, g.bmean, g.out,
+            g.out_lo, g.ld);
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_chan_prepare(const MeanSet& ms, const long long* n_dev, const int* nb, float* f,
+cudaError_t launch_chan_prepare(const MeanSet& ms, const long long* n_dev, const int* nb, float* coef,
                                 cudaStream_t s) {
-    chan_prepare_kernel<<<256, 256, 0, s>>>(ms, n_dev, nb, f);
+    chan_prepare_kernel<<<256, 256, 0, s>>>(ms, n_dev, nb, coef);
     return cudaGetLastError();
 }
 
@@ -545,20 +581,20 @@ cudaError_t launch_chan_finish(long long* n_dev, const int* nb, cudaStream_t s) 
 }
 
 cudaError_t launch_syy(const void* Y, const void* Ylo, int64_t ld, int64_t rows_n, const int* nb, const float* dy,
-                       const float* f, float* syy, cudaStream_t s) {
+                       const float* zy, const float* coef, float* syy, cudaStream_t s) {
     const int64_t threads = rows_n * 32;
     const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
     if (blocks == 0) return cudaSuccess;
-    syy_kernel<<<blocks, 256, 0, s>>>(Y, Ylo, ld, rows_n, nb, dy, f, syy);
+    syy_kernel<<<blocks, 256, 0, s>>>(Y, Ylo, ld, rows_n, nb, dy, zy, coef, syy);
     return cudaGetLastError();
 }
 
 cudaError_t launch_stats_gemm_simt(const float* A, const float* B, int64_t ld, int64_t Ma, int64_t Nb, bool lower,
-                                   const float* da, const float* db, const float* f, const int* nb, float* out,
-                                   int64_t ldo, cudaStream_t s) {
+                                   const float* da, const float* db, const float* za, const float* zb,
+                                   const float* coef, const int* nb, float* out, int64_t ldo, cudaStream_t s) {
     dim3 grid(static_cast<unsigned>((Nb + 63) / 64), static_cast<unsigned>((Ma + 63) / 64));
     if (grid.x == 0 || grid.y == 0) return cudaSuccess;
-    stats_gemm_simt_kernel<<<grid, 256, 0, s>>>(A, B, ld, Ma, Nb, lower ? 1 : 0, da, db, f, nb, out, ldo);
+    stats_gemm_simt_kernel<<<grid, 256, 0, s>>>(A, B, ld, Ma, Nb, lower ? 1 : 0, da, db, za, zb, coef, nb, out, ldo);
     return cudaGetLastError();
 }
 

@@ -21,12 +21,15 @@ struct kvb_stats {
     int64_t Fs = 0, Ft = 0;     // all source features, all target columns
     long long* n_dev = nullptr;
     int* nb_dev = nullptr;
-    float* f_dev = nullptr;
+    float* coef_dev = nullptr;  // {f = n_a n_b / n, g = n_b} of the current batch
     int* rows = nullptr;
     float* mean[4] = {};   // running means: source K, source V, target K, target V
-    float* bmean[4] = {};  // batch means
+    float* bmean[4] = {};  // batch means (generic gather)
     float* delta[4] = {};  // batch mean - running mean before the merge
-    float* bpart = nullptr;  // [8][max(Fs, Ft)] partial column sums of one matrix
+    float* zbar[4] = {};   // mean of the shifted batch (0 on the generic gather)
+    float* zsum[4] = {};   // column sums of the shifted batch (single-pass gather)
+    float* shift[4] = {};  // shift of the batch (single-pass gather)
+    float* part = nullptr; // [ld/64][max(Fs, Ft)] per-chunk column sums of one matrix
     float* gram[2] = {};   // [Fs][Fs], lower triangle kept
     float* cross[2] = {};  // [Fs][Ft]
     float* syy[2] = {};    // [Ft]
@@ -109,6 +112,8 @@ void stats_jobs(const kvb_stats* st, StatsJob jobs[4]) {
         g.out = st->gram[kv];
         g.da = st->delta[kv];
         g.db = st->delta[kv];
+        g.za = st->zbar[kv];
+        g.zb = st->zbar[kv];
         g.Ma = st->Fs;
         g.Nb = st->Fs;
         g.ldo = st->Fs;
@@ -121,6 +126,8 @@ void stats_jobs(const kvb_stats* st, StatsJob jobs[4]) {
         x.out = st->cross[kv];
         x.da = st->delta[kv];
         x.db = st->delta[2 + kv];
+        x.za = st->zbar[kv];
+        x.zb = st->zbar[2 + kv];
         x.Ma = st->Fs;
         x.Nb = st->Ft;
         x.ldo = st->Ft;
@@ -157,7 +164,7 @@ kvb_status kvb_stats_create(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_batch_tok
     st->ctx = ctx;
     st->dtype = dtype;
     st->max_T = max_batch_tokens;
-    st->ld = (max_batch_tokens + 63) & ~int64_t(63);
+    st->ld = (max_batch_tokens + 127) & ~int64_t(127);  // whole 128-row gather chunks
     const int64_t q = static_cast<int64_t>(ctx->H) * ctx->d;
     st->Fs = ctx->L_s * q;
     st->Ft = ctx->L_t * q;
@@ -167,7 +174,7 @@ kvb_status kvb_stats_create(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_batch_tok
     };
     A(reinterpret_cast<void**>(&st->n_dev), sizeof(long long));
     A(reinterpret_cast<void**>(&st->nb_dev), sizeof(int));
-    A(reinterpret_cast<void**>(&st->f_dev), sizeof(float));
+    A(reinterpret_cast<void**>(&st->coef_dev), 2 * sizeof(float));
     A(reinterpret_cast<void**>(&st->numeric), sizeof(int));
     A(reinterpret_cast<void**>(&st->rows), st->max_T * sizeof(int));
     const int64_t len[4] = {st->Fs, st->Fs, st->Ft, st->Ft};
@@ -175,6 +182,9 @@ kvb_status kvb_stats_create(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_batch_tok
         A(reinterpret_cast<void**>(&st->mean[m]), len[m] * 4);
         A(reinterpret_cast<void**>(&st->bmean[m]), len[m] * 4);
         A(reinterpret_cast<void**>(&st->delta[m]), len[m] * 4);
+        A(reinterpret_cast<void**>(&st->zbar[m]), len[m] * 4);
+        A(reinterpret_cast<void**>(&st->zsum[m]), len[m] * 4);
+        A(reinterpret_cast<void**>(&st->shift[m]), len[m] * 4);
     }
     for (int kv = 0; kv < 2; ++kv) {
         A(reinterpret_cast<void**>(&st->gram[kv]), static_cast<size_t>(st->Fs) * st->Fs * 4);
@@ -198,7 +208,7 @@ kvb_status kvb_stats_create(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_batch_tok
             A(&st->YT[kv], static_cast<size_t>(st->Ft) * st->ld * 4);
         }
     }
-    A(reinterpret_cast<void**>(&st->bpart), 8ull * std::max(st->Fs, st->Ft) * 4);
+    A(reinterpret_cast<void**>(&st->part), static_cast<size_t>(st->ld / 128) * std::max(st->Fs, st->Ft) * 4);
     A(reinterpret_cast<void**>(&st->r2), 2ull * ctx->L_t * ctx->L_s * 4);
     A(reinterpret_cast<void**>(&st->sel), 2ull * ctx->L_t * ctx->k * 4);
     if (s == KVB_OK) s = zero_stats(st, 0);
@@ -267,21 +277,42 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
     if (e != cudaSuccess) return cuda_fail(e, "row selection");
     {
         ProfScope ps(c, cs, "calib_gather_center");
-        for (int m = 0; m < 4 && e == cudaSuccess; ++m)
-            e = launch_colmean(dt, caches[m], slabs[m], T, c->d, st->rows, st->nb_dev, positions, tabs[m],
-                               tabs[m] != nullptr, st->bmean[m], st->bpart, cs);
+        const bool single = gather_single_pass_ok(dt, c->d);
+        for (int m = 0; m < 4 && e == cudaSuccess; ++m) {
+            GatherArgs g{};
+            g.dt = dt;
+            g.cache = caches[m];
+            g.n_slabs = slabs[m];
+            g.T = T;
+            g.d = c->d;
+            g.rows = st->rows;
+            g.nb = st->nb_dev;
+            g.n_seen = st->n_dev;
+            g.pos = positions;
+            g.tab = tabs[m];
+            g.strip = tabs[m] != nullptr;
+            g.mean_a = st->mean[m];
+            g.shift = st->shift[m];
+            g.part = st->part;
+            g.zsum = st->zsum[m];
+            g.bmean = st->bmean[m];
+            g.out = outs[m];
+            g.out_lo = outs_lo[m];
+            g.ld = st->ld;
+            e = launch_gather(g, cs);
+        }
         MeanSet ms;
         for (int m = 0; m < 4; ++m) {
             ms.mean[m] = st->mean[m];
             ms.bmean[m] = st->bmean[m];
+            ms.zsum[m] = single ? st->zsum[m] : nullptr;
+            ms.shift[m] = single ? st->shift[m] : nullptr;
             ms.delta[m] = st->delta[m];
+            ms.zbar[m] = st->zbar[m];
         }
         ms.len[0] = ms.len[1] = st->Fs;
         ms.len[2] = ms.len[3] = st->Ft;
-        if (e == cudaSuccess) e = launch_chan_prepare(ms, st->n_dev, st->nb_dev, st->f_dev, cs);
-        for (int m = 0; m < 4 && e == cudaSuccess; ++m)
-            e = launch_center_transpose(dt, caches[m], slabs[m], T, c->d, st->rows, st->nb_dev, positions, tabs[m],
-                                        tabs[m] != nullptr, st->bmean[m], outs[m], outs_lo[m], st->ld, cs);
+        if (e == cudaSuccess) e = launch_chan_prepare(ms, st->n_dev, st->nb_dev, st->coef_dev, cs);
     }
     if (e != cudaSuccess) return cuda_fail(e, "gather/center");
     StatsJob jobs[4];
@@ -289,21 +320,21 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
     if (st->use_tc) {
         std::string why;
         ProfScope ps(c, cs, "stats_gemm_tcgen05");
-        e = launch_stats_gemm_tc(st->plan, jobs, 4, st->ld, st->f_dev, st->nb_dev, err, c->num_sms, cs, &why);
+        e = launch_stats_gemm_tc(st->plan, jobs, 4, st->ld, st->coef_dev, st->nb_dev, err, c->num_sms, cs, &why);
         if (e != cudaSuccess && !why.empty()) return fail(KVB_ERR_CUDA, "statistics GEMM: " + why);
     } else {
         ProfScope ps(c, cs, "stats_gemm_simt");
         for (int j = 0; j < 4 && e == cudaSuccess; ++j)
             e = launch_stats_gemm_simt(static_cast<const float*>(jobs[j].A), static_cast<const float*>(jobs[j].B),
                                        st->ld, jobs[j].Ma, jobs[j].Nb, jobs[j].lower != 0, jobs[j].da, jobs[j].db,
-                                       st->f_dev, st->nb_dev, jobs[j].out, jobs[j].ldo, cs);
+                                       jobs[j].za, jobs[j].zb, st->coef_dev, st->nb_dev, jobs[j].out, jobs[j].ldo, cs);
     }
     if (e != cudaSuccess) return cuda_fail(e, "statistics GEMM");
     {
         ProfScope ps(c, cs, "calib_syy_merge");
         for (int kv = 0; kv < 2 && e == cudaSuccess; ++kv)
-            e = launch_syy(st->YT[kv], st->YT_lo[kv], st->ld, st->Ft, st->nb_dev, st->delta[2 + kv], st->f_dev,
-                           st->syy[kv], cs);
+            e = launch_syy(st->YT[kv], st->YT_lo[kv], st->ld, st->Ft, st->nb_dev, st->delta[2 + kv], st->zbar[2 + kv],
+                           st->coef_dev, st->syy[kv], cs);
         if (e == cudaSuccess) e = launch_chan_finish(st->n_dev, st->nb_dev, cs);
     }
     if (e != cudaSuccess) return cuda_fail(e, "S_yy / merge");

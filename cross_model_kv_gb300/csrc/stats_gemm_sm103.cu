@@ -3,9 +3,10 @@
 // Every job is a centered cross-product over the observations of one batch,
 // merged into the running statistics with Chan's update ("KVBridge" README,
 // "Loading"):
-//     out[i][j] += sum_r A[i][r] B[j][r] + f da[i] db[j]
-// with A, B the centered, transposed batch ([feature][observation], K-major)
-// and f da db the rank-1 mean-shift term.  The operands are bf16 pairs
+//     out[i][j] += sum_r A[i][r] B[j][r] - g za[i] zb[j] + f da[i] db[j]
+// with A, B the shifted, transposed batch ([feature][observation], K-major),
+// g za zb the rank-1 term that centers it on the batch mean and f da db the
+// rank-1 Chan term between the running and the batch means.  The operands are bf16 pairs
 // (hi + lo) of the float32 centered values; the product is accumulated as
 // hi.hi + hi.lo + lo.hi in one fp32 TMEM accumulator, three K-passes over the
 // same tile, which keeps ~16 significant bits per operand.
@@ -51,6 +52,8 @@ struct JobP {
     float* out;
     const float* da;
     const float* db;
+    const float* za;
+    const float* zb;
     int64_t ldo;
 };
 
@@ -58,7 +61,7 @@ struct Params {
     const uint32_t* tiles;
     int n_tiles;
     const int* nb;
-    const float* f;
+    const float* coef;  // {f, g}
     DevErr err;
     JobP job[4];
 };
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int sub = warp & 3;          // TMEM lane quarter
         const int colhalf = ew >> 2;       // columns [0,128) or [128,256)
         const int row = sub * 32 + lane;
-        const float ff = *P.f;
+        const float ff = P.coef[0], gg = P.coef[1];
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < P.n_tiles; t += gridDim.x) {
@@ -202,7 +205,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t j0 = static_cast<int64_t>(bj) * BN + colhalf * 128;
             float* orow = J.out + i * J.ldo + j0;
             const float fda = ff * __ldg(J.da + i);
+            const float gza = gg * __ldg(J.za + i);
             const float* dbp = J.db + j0;
+            const float* zbp = J.zb + j0;
             if (iters > 0) {
                 if (!mbar_wait(&tfull[acc], acc_phase, P.err, abort_flag)) break;
                 tc_fence_after();
@@ -230,11 +235,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const float4 d = __ldg(reinterpret_cast<const float4*>(dbp + c0 + 4 * v));
+                    const float4 z = __ldg(reinterpret_cast<const float4*>(zbp + c0 + 4 * v));
                     float4 o = cur[v];
-                    o.x += __uint_as_float(r[4 * v + 0]) + fda * d.x;
-                    o.y += __uint_as_float(r[4 * v + 1]) + fda * d.y;
-                    o.z += __uint_as_float(r[4 * v + 2]) + fda * d.z;
-                    o.w += __uint_as_float(r[4 * v + 3]) + fda * d.w;
+                    o.x += __uint_as_float(r[4 * v + 0]) + fda * d.x - gza * z.x;
+                    o.y += __uint_as_float(r[4 * v + 1]) + fda * d.y - gza * z.y;
+                    o.z += __uint_as_float(r[4 * v + 2]) + fda * d.z - gza * z.z;
+                    o.w += __uint_as_float(r[4 * v + 3]) + fda * d.w - gza * z.w;
                     *reinterpret_cast<float4*>(orow + c0 + 4 * v) = o;
                 }
                 if (c0 + 16 < 128) {
@@ -326,8 +332,9 @@ void stats_gemm_tc_free(StatsGemmPlan* plan) {
     delete plan;
 }
 
-cudaError_t launch_stats_gemm_tc(StatsGemmPlan* plan, const StatsJob* jobs, int n_jobs, int64_t ld, const float* f,
-                                 const int* nb, DevErr err, int num_sms, cudaStream_t s, std::string* why) {
+cudaError_t launch_stats_gemm_tc(StatsGemmPlan* plan, const StatsJob* jobs, int n_jobs, int64_t ld,
+                                 const float* coef, const int* nb, DevErr err, int num_sms, cudaStream_t s,
+                                 std::string* why) {
     if (!plan || plan->n_tiles == 0) return cudaSuccess;
     Maps M;
     std::memset(&M, 0, sizeof(M));
@@ -335,14 +342,14 @@ cudaError_t launch_stats_gemm_tc(StatsGemmPlan* plan, const StatsJob* jobs, int 
     P.tiles = plan->tiles;
     P.n_tiles = plan->n_tiles;
     P.nb = nb;
-    P.f = f;
+    P.coef = coef;
     P.err = err;
     for (int j = 0; j < n_jobs; ++j) {
         const StatsJob& J = jobs[j];
         if (!encode_2d(&M.a_hi[j], J.A, ld, J.Ma, BM, why) || !encode_2d(&M.a_lo[j], J.A_lo, ld, J.Ma, BM, why) ||
             !encode_2d(&M.b_hi[j], J.B, ld, J.Nb, BN, why) || !encode_2d(&M.b_lo[j], J.B_lo, ld, J.Nb, BN, why))
             return cudaErrorInvalidValue;
-        P.job[j] = JobP{J.out, J.da, J.db, J.ldo};
+        P.job[j] = JobP{J.out, J.da, J.db, J.za, J.zb, J.ldo};
     }
     cudaError_t e = cudaFuncSetAttribute(stats_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;

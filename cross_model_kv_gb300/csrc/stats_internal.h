@@ -6,36 +6,57 @@
 namespace kvb {
 
 // Four running-mean vectors: source keys, source values, target keys, target values.
+// zsum/shift are set (single-pass path) or NULL (generic path, bmean used).
 struct MeanSet {
     float* mean[4];
     const float* bmean[4];
+    const float* zsum[4];
+    const float* shift[4];
     float* delta[4];
+    float* zbar[4];
     int64_t len[4];
 };
 
+// One matrix of one batch: kept rows of `cache` [n_slabs][T][d] -> centered,
+// transposed operand out ([n_slabs*d][ld]; float32, or bf16 hi/lo if out_lo).
+struct GatherArgs {
+    kvb_dtype dt;
+    const void* cache;
+    int64_t n_slabs, T;
+    int d;
+    const int* rows;
+    const int* nb;
+    const long long* n_seen;  // observations merged before this batch
+    const int* pos;
+    const float2* tab;        // RoPE table (keys), or NULL
+    bool strip;
+    const float* mean_a;      // running mean before the batch (single-pass shift)
+    float* shift;             // [n_slabs*d] shift used (single-pass path)
+    float* part;              // [T/64][n_slabs*d] per-chunk column sums (single-pass path)
+    float* zsum;              // [n_slabs*d] column sums of z (single-pass path)
+    float* bmean;             // [n_slabs*d] batch mean (generic path)
+    void* out;
+    void* out_lo;
+    int64_t ld;
+};
+bool gather_single_pass_ok(kvb_dtype dt, int d);
+cudaError_t launch_gather(const GatherArgs& g, cudaStream_t s);
+
 cudaError_t launch_select_rows(const int* pos, int64_t T, int stride, int max_pos, int* rows, int* nb, DevErr err,
                                cudaStream_t s);
-// Batch column means.  `part` ([8][n_slabs*d] floats) enables the vectorised
-// bf16 path (head_dim % 16 == 0); NULL forces the generic kernel.
-cudaError_t launch_colmean(kvb_dtype dt, const void* cache, int64_t n_slabs, int64_t T, int d, const int* rows,
-                           const int* nb, const int* pos, const float2* tab, bool strip, float* mean, float* part,
-                           cudaStream_t s);
-// out_lo == nullptr: float32 output; otherwise the (hi, lo) bf16 split into out / out_lo.
-cudaError_t launch_center_transpose(kvb_dtype dt, const void* cache, int64_t n_slabs, int64_t T, int d,
-                                    const int* rows, const int* nb, const int* pos, const float2* tab, bool strip,
-                                    const float* mean, void* out, void* out_lo, int64_t ld, cudaStream_t s);
-cudaError_t launch_chan_prepare(const MeanSet& ms, const long long* n_dev, const int* nb, float* f,
+// coef = {f = n_a n_b / n, g = n_b}
+cudaError_t launch_chan_prepare(const MeanSet& ms, const long long* n_dev, const int* nb, float* coef,
                                 cudaStream_t s);
 cudaError_t launch_symmetrize(const float* src, float* dst, int64_t n, cudaStream_t s);
 cudaError_t launch_chan_finish(long long* n_dev, const int* nb, cudaStream_t s);
 cudaError_t launch_syy(const void* Y, const void* Ylo, int64_t ld, int64_t rows_n, const int* nb, const float* dy,
-                       const float* f, float* syy, cudaStream_t s);
+                       const float* zy, const float* coef, float* syy, cudaStream_t s);
 cudaError_t launch_stats_gemm_simt(const float* A, const float* B, int64_t ld, int64_t Ma, int64_t Nb, bool lower,
-                                   const float* da, const float* db, const float* f, const int* nb, float* out,
-                                   int64_t ldo, cudaStream_t s);
+                                   const float* da, const float* db, const float* za, const float* zb,
+                                   const float* coef, const int* nb, float* out, int64_t ldo, cudaStream_t s);
 
 // Statistics GEMM jobs, K = observations:
-//   out[i][j] += sum_r A[i][r] B[j][r] + f da[i] db[j].
+//   out[i][j] += sum_r A[i][r] B[j][r] - g za[i] zb[j] + f da[i] db[j].
 // CUDA-core path: A, B float32 [rows][ld].  Tensor-core path: A = A + A_lo and
 // B = B + B_lo as bf16 pairs; the product is taken as A.B + A.B_lo + A_lo.B
 // (three bf16 passes into one fp32 accumulator; A_lo.B_lo is below fp32 noise).
@@ -47,6 +68,8 @@ struct StatsJob {
     float* out;      // [Ma][ldo]
     const float* da;
     const float* db;
+    const float* za;
+    const float* zb;
     int64_t Ma, Nb, ldo;
     int lower;       // only tiles touching the lower triangle (j <= i)
 };
@@ -55,7 +78,7 @@ bool stats_gemm_tc_supported(const StatsJob* jobs, int n_jobs);
 cudaError_t stats_gemm_tc_plan(const StatsJob* jobs, int n_jobs, StatsGemmPlan** plan);
 void stats_gemm_tc_free(StatsGemmPlan* plan);
 cudaError_t launch_stats_gemm_tc(StatsGemmPlan* plan, const StatsJob* jobs, int n_jobs, int64_t ld,
-                                 const float* f, const int* nb, DevErr err, int num_sms, cudaStream_t s,
+                                 const float* coef, const int* nb, DevErr err, int num_sms, cudaStream_t s,
                                  std::string* why);
 
 // ---------------------------------------------------------------- dense solves (fp32, batched)

@@ -363,7 +363,7 @@ def run_gpu(args, rank, world, local_rank):
     if args.skip_extras:
         if rank == 0:
             print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s", "ms_per_step": ms_per_step,
-                              "workload": args.workload, "kernels": kernels}), flush=True)
+                              "workload": args.workload, "kernels": kernels, "clocks": clk}), flush=True)
         return
 
     # ---------------- end to end: pinned host buffers, copies inside the timed region.

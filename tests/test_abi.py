@@ -92,3 +92,10 @@ def _load_missing(tmp_path):
         _binding.load_library(str(tmp_path / "missing.so"))
     finally:
         _binding._lib = saved
+
+
+def test_binding_rejects_wrong_selection_shape_before_the_library():
+    import numpy as np
+    from cross_model_kv_gb300 import _binding
+    with pytest.raises(ValueError, match="selection"):
+        _binding._host_sel(np.zeros((3, 2), dtype=np.int32), 4, 2)

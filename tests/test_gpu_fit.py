@@ -257,3 +257,54 @@ def test_qwen3_14b_to_32b_calibration_pass_sampled(kvb):
         got = np.array([r2h[kv, t_star, pair[0]], r2h[kv, t_star, pair[1]]])
         assert np.max(np.abs(got - ref)) < 1e-4, (got, ref)
         assert ref[0] > ref[1] + 0.02
+
+
+def test_no_observations_and_zero_lambda_is_a_numeric_error(kvb):
+    # Nothing accumulated and lambda = 0: every system is zero, not positive definite.
+    pair = make_pair(21, 3, 2, 2, 16, 2, 64, 1, 1e4, 1e6)
+    ctx = _ctx(kvb, pair, 64)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 64)
+    with pytest.raises(kvb.KvbError) as e:
+        kvb.kvb_layer_select(ctx, st, 0.0)
+    assert e.value.status == 5
+    Wk = torch.empty((2, 32, 64), dtype=torch.float32, device="cuda")
+    bk = torch.empty((2, 32), dtype=torch.float32, device="cuda")
+    sel = np.array([[0, 1], [1, 2]], dtype=np.int32)
+    with pytest.raises(kvb.KvbError) as e:
+        kvb.kvb_ridge_solve(ctx, st, sel, sel, 0.0, Wk, Wk.clone(), bk, bk.clone())
+    assert e.value.status == 5
+
+
+def test_top_k_equal_to_all_source_layers(kvb):
+    # k = L_src: every source layer is selected; the fit uses all of them.
+    pair = make_pair(22, 3, 2, 2, 16, 3, 256, 4, 1e4, 5e4)
+    ctx = _ctx(kvb, pair, 256)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 256)
+    _accumulate(kvb, ctx, st, pair["calib"], torch.float32)
+    sel_k, sel_v, r2, Wk, Wv, bk, bv = _run_fit(kvb, ctx, st, pair, torch.float32)
+    assert sel_k.tolist() == [[0, 1, 2]] * 2 and sel_v.tolist() == [[0, 1, 2]] * 2
+    fit = O.fit_mapper(pair["calib"], 1e4, 5e4, 3, 0.01, 4)
+    assert rel_fro(np.transpose(to_host64(Wk), (0, 2, 1)), fit.W_k) < 1e-4
+
+
+@pytest.mark.parametrize("stride", [1, 3, 7])
+def test_other_strides(kvb, stride):
+    pair = make_pair(23, 3, 2, 2, 16, 2, 100, 3, 1e4, 1e6)
+    ctx = _ctx(kvb, pair, 128)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 128)
+    _accumulate(kvb, ctx, st, pair["calib"], torch.float32, stride=stride)
+    ref = oracle_full_stats(pair, stride)
+    for kv in (0, 1):
+        n, mx, my, g, c, y = _export(kvb, st, kv, 96, 64)
+        assert n == ref[kv].n and rel_fro(g, ref[kv].M) < 1e-5 and rel_fro(c, ref[kv].C) < 1e-5
+
+
+def test_reset_then_accumulate_again(kvb):
+    pair = round_pair(make_pair(24, 2, 2, 2, 128, 1, 512, 2, 1e4, 1e6, sigma=1.0), torch.bfloat16)
+    ctx = _ctx(kvb, pair, 512)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, 512)
+    _accumulate(kvb, ctx, st, pair["calib"][::-1], torch.bfloat16)  # other order first
+    kvb.kvb_stats_reset(st)
+    assert kvb.kvb_stats_count(st) == 0
+    _accumulate(kvb, ctx, st, pair["calib"], torch.bfloat16)
+    _check_stats(kvb, st, pair, 1e-4)

@@ -92,9 +92,128 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const GemmArgs g) {
     }
 }
 
+// Vectorised, double-buffered variant for K % 16 == 0, M and N % 4 == 0 and
+// 16-byte aligned operands: 16-byte global loads along the contiguous index of
+// A (K or M) and of B (N or K), the next K-slice fetched into registers while
+// the current one is multiplied out of shared memory.
+template <bool A_KCONTIG, bool B_NCONTIG>
+__global__ void __launch_bounds__(256, 2) gemm_f32_vec_kernel(const GemmArgs g) {
+    constexpr int BKV = 16;
+    __shared__ __align__(16) float As[2][BKV][GB + 4];
+    __shared__ __align__(16) float Bs[2][BKV][GB + 4];
+    const int b = blockIdx.z;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * GB;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * GB;
+    if (g.lower && n0 > m0 + GB - 1) return;
+    const float* A = g.A + b * g.strideA;
+    const float* B = g.B + b * g.strideB;
+    float* C = g.C + b * g.strideC;
+    const int tid = threadIdx.x;
+    const int tx = tid & 15, ty = tid >> 4;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 ra[2], rb[2];
+
+    auto load = [&](int64_t k0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int e = tid + i * 256;
+            if (A_KCONTIG) {
+                const int64_t gm = m0 + (e >> 2), gk = k0 + (e & 3) * 4;
+                ra[i] = (gm < g.M && gk < g.K) ? __ldg(reinterpret_cast<const float4*>(A + gm * g.sam + gk)) : zero;
+            } else {
+                const int64_t gk = k0 + (e >> 5), gm = m0 + (e & 31) * 4;
+                ra[i] = (gm < g.M && gk < g.K) ? __ldg(reinterpret_cast<const float4*>(A + gk * g.sak + gm)) : zero;
+            }
+            if (B_NCONTIG) {
+                const int64_t gk = k0 + (e >> 5), gn = n0 + (e & 31) * 4;
+                rb[i] = (gn < g.N && gk < g.K) ? __ldg(reinterpret_cast<const float4*>(B + gk * g.sbk + gn)) : zero;
+            } else {
+                const int64_t gn = n0 + (e >> 2), gk = k0 + (e & 3) * 4;
+                rb[i] = (gn < g.N && gk < g.K) ? __ldg(reinterpret_cast<const float4*>(B + gn * g.sbn + gk)) : zero;
+            }
+        }
+    };
+    auto store = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int e = tid + i * 256;
+            if (A_KCONTIG) {
+                const int mm = e >> 2, kk = (e & 3) * 4;
+                As[buf][kk + 0][mm] = ra[i].x;
+                As[buf][kk + 1][mm] = ra[i].y;
+                As[buf][kk + 2][mm] = ra[i].z;
+                As[buf][kk + 3][mm] = ra[i].w;
+            } else {
+                *reinterpret_cast<float4*>(&As[buf][e >> 5][(e & 31) * 4]) = ra[i];
+            }
+            if (B_NCONTIG) {
+                *reinterpret_cast<float4*>(&Bs[buf][e >> 5][(e & 31) * 4]) = rb[i];
+            } else {
+                const int nn = e >> 2, kk = (e & 3) * 4;
+                Bs[buf][kk + 0][nn] = rb[i].x;
+                Bs[buf][kk + 1][nn] = rb[i].y;
+                Bs[buf][kk + 2][nn] = rb[i].z;
+                Bs[buf][kk + 3][nn] = rb[i].w;
+            }
+        }
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    load(0);
+    store(0);
+    __syncthreads();
+    int buf = 0;
+    for (int64_t k0 = 0; k0 < g.K; k0 += BKV) {
+        const bool more = k0 + BKV < g.K;
+        if (more) load(k0 + BKV);
+#pragma unroll
+        for (int kk = 0; kk < BKV; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4 + 64]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4 + 64]);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+        }
+        if (more) store(buf ^ 1);
+        __syncthreads();
+        buf ^= 1;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t gm = m0 + ty * 4 + (i & 3) + (i >> 2) * 64;
+        if (gm >= g.M) continue;
+#pragma unroll
+        for (int jh = 0; jh < 2; ++jh) {
+            const int64_t gn = n0 + tx * 4 + jh * 64;
+            if (gn >= g.N) continue;
+            float4* p = reinterpret_cast<float4*>(C + gm * g.ldc + gn);
+            float4 v = make_float4(g.alpha * acc[i][4 * jh + 0], g.alpha * acc[i][4 * jh + 1],
+                                   g.alpha * acc[i][4 * jh + 2], g.alpha * acc[i][4 * jh + 3]);
+            if (g.beta != 0.f) {
+                const float4 o = *p;
+                v.x = fmaf(g.beta, o.x, v.x);
+                v.y = fmaf(g.beta, o.y, v.y);
+                v.z = fmaf(g.beta, o.z, v.z);
+                v.w = fmaf(g.beta, o.w, v.w);
+            }
+            *p = v;
+        }
+    }
+}
+
 // Cholesky of the nb x nb diagonal block at (k0, k0), in shared memory.  One CTA per system.
 __global__ void __launch_bounds__(256) potrf_diag_kernel(float* G, int64_t ldg, int64_t strideG, int64_t k0,
-                                                         int nb, int* numeric_flag) {
+                                                         int nb, int* numeric_flag, float* Linv, int64_t strideL) {
     __shared__ float a[NB][NB + 1];
     float* Gb = G + blockIdx.x * strideG + k0 * ldg + k0;
     for (int e = threadIdx.x; e < nb * nb; e += blockDim.x) {
@@ -127,60 +246,23 @@ __global__ void __launch_bounds__(256) potrf_diag_kernel(float* G, int64_t ldg, 
         const int i = e / nb, j = e % nb;
         Gb[i * ldg + j] = j <= i ? a[i][j] : 0.f;
     }
-}
-
-// Panel below the diagonal block: P <- P L_kk^-T (rows independent).  Thread per row.
-__global__ void trsm_panel_kernel(float* G, int64_t ldg, int64_t strideG, int64_t k0, int nb, int64_t rows) {
-    __shared__ float L[NB][NB + 1];
-    float* Gs = G + blockIdx.y * strideG;
-    for (int e = threadIdx.x; e < nb * nb; e += blockDim.x) {
-        const int i = e / nb, j = e % nb;
-        L[i][j] = Gs[(k0 + i) * ldg + k0 + j];
-    }
-    __syncthreads();
-    const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    if (r >= rows) return;
-    float* row = Gs + (k0 + nb + r) * ldg + k0;
-    float x[NB];
-#pragma unroll 4
-    for (int j = 0; j < nb; ++j) {
-        float v = row[j];
-        for (int k = 0; k < j; ++k) v = fmaf(-x[k], L[j][k], v);
-        x[j] = v / L[j][j];
-    }
-    for (int j = 0; j < nb; ++j) row[j] = x[j];
-}
-
-// Block row k0..k0+nb of C: forward (L_kk Y = C_k) or backward (L_kk^T X = Y_k).
-// Thread per right-hand-side column.
-__global__ void trsm_rhs_kernel(const float* L, int64_t ldg, int64_t strideG, int64_t k0, int nb, float* C,
-                                int64_t ldc, int64_t strideC, int64_t m, int backward) {
-    __shared__ float Ls[NB][NB + 1];
-    const float* Lb = L + blockIdx.y * strideG;
-    for (int e = threadIdx.x; e < nb * nb; e += blockDim.x) {
-        const int i = e / nb, j = e % nb;
-        Ls[i][j] = Lb[(k0 + i) * ldg + k0 + j];
-    }
-    __syncthreads();
-    const int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    if (c >= m) return;
-    float* col = C + blockIdx.y * strideC + k0 * ldc + c;
-    float y[NB];
-    for (int i = 0; i < nb; ++i) y[i] = col[i * ldc];
-    if (!backward) {
-        for (int i = 0; i < nb; ++i) {
-            float v = y[i];
-            for (int k = 0; k < i; ++k) v = fmaf(-Ls[i][k], y[k], v);
-            y[i] = v / Ls[i][i];
+    // Inverse of the lower-triangular factor, column j by forward substitution
+    // (one thread per column), stored as a dense NB x NB block.
+    float* Li = Linv + blockIdx.x * strideL + k0 * NB;
+    if (threadIdx.x < NB) {
+        const int j = threadIdx.x;
+        float x[NB];
+        for (int i = 0; i < NB; ++i) {
+            float v = 0.f;
+            if (i < nb && i >= j) {
+                v = i == j ? 1.f : 0.f;
+                for (int k = j; k < i; ++k) v = fmaf(-a[i][k], x[k], v);
+                v /= a[i][i];
+            }
+            x[i] = v;
         }
-    } else {
-        for (int i = nb - 1; i >= 0; --i) {
-            float v = y[i];
-            for (int k = i + 1; k < nb; ++k) v = fmaf(-Ls[k][i], y[k], v);
-            y[i] = v / Ls[i][i];
-        }
+        for (int i = 0; i < NB; ++i) Li[i * NB + j] = x[i];
     }
-    for (int i = 0; i < nb; ++i) col[i * ldc] = y[i];
 }
 
 }  // namespace
@@ -188,19 +270,53 @@ __global__ void trsm_rhs_kernel(const float* L, int64_t ldg, int64_t strideG, in
 cudaError_t launch_gemm_f32(const GemmArgs& g, cudaStream_t s) {
     if (g.M <= 0 || g.N <= 0 || g.batch <= 0) return cudaSuccess;
     dim3 grid(static_cast<unsigned>((g.N + GB - 1) / GB), static_cast<unsigned>((g.M + GB - 1) / GB), g.batch);
-    gemm_f32_kernel<<<grid, 256, 0, s>>>(g);
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const bool a_k = g.sak == 1, a_m = g.sam == 1, b_n = g.sbn == 1, b_k = g.sbk == 1;
+    const int64_t sa = a_k ? g.sam : g.sak, sb = b_n ? g.sbk : g.sbn;
+    const bool vec = g.K % 16 == 0 && g.M % 4 == 0 && g.N % 4 == 0 && (a_k || a_m) && (b_n || b_k) && sa % 4 == 0 &&
+                     sb % 4 == 0 && g.ldc % 4 == 0 && g.strideA % 4 == 0 && g.strideB % 4 == 0 &&
+                     g.strideC % 4 == 0 && al16(g.A) && al16(g.B) && al16(g.C);
+    if (!vec) {
+        gemm_f32_kernel<<<grid, 256, 0, s>>>(g);
+    } else if (a_k && b_n) {
+        gemm_f32_vec_kernel<true, true><<<grid, 256, 0, s>>>(g);
+    } else if (a_k) {
+        gemm_f32_vec_kernel<true, false><<<grid, 256, 0, s>>>(g);
+    } else if (b_n) {
+        gemm_f32_vec_kernel<false, true><<<grid, 256, 0, s>>>(g);
+    } else {
+        gemm_f32_vec_kernel<false, false><<<grid, 256, 0, s>>>(g);
+    }
     return cudaGetLastError();
 }
 
 cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t n, int batch, int* numeric_flag,
-                                cudaStream_t s) {
+                                float* Linv, int64_t strideL, cudaStream_t s) {
     for (int64_t k0 = 0; k0 < n; k0 += NB) {
         const int nb = static_cast<int>(n - k0 < NB ? n - k0 : NB);
-        potrf_diag_kernel<<<batch, 256, 0, s>>>(G, ldg, strideG, k0, nb, numeric_flag);
+        potrf_diag_kernel<<<batch, 256, 0, s>>>(G, ldg, strideG, k0, nb, numeric_flag, Linv, strideL);
         const int64_t rem = n - k0 - nb;
         if (rem <= 0) continue;
-        dim3 tg(static_cast<unsigned>((rem + 127) / 128), batch);
-        trsm_panel_kernel<<<tg, 128, 0, s>>>(G, ldg, strideG, k0, nb, rem);
+        // panel below the diagonal block: P <- P L_kk^-T (rows independent, in place)
+        GemmArgs t{};
+        t.A = G + (k0 + nb) * ldg + k0;
+        t.B = Linv + k0 * NB;  // B(k, n) = Linv[n][k]
+        t.C = G + (k0 + nb) * ldg + k0;
+        t.sam = ldg;
+        t.sak = 1;
+        t.sbk = 1;
+        t.sbn = NB;
+        t.ldc = ldg;
+        t.strideA = t.strideC = strideG;
+        t.strideB = strideL;
+        t.M = rem;
+        t.N = nb;
+        t.K = nb;
+        t.alpha = 1.f;
+        t.beta = 0.f;
+        t.batch = batch;
+        cudaError_t e = launch_gemm_f32(t, s);
+        if (e != cudaSuccess) return e;
         GemmArgs g{};
         g.A = G + (k0 + nb) * ldg + k0;  // P: rem x nb
         g.B = G + (k0 + nb) * ldg + k0;  // P^T: B(k, n) = P[n][k]
@@ -217,19 +333,42 @@ cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t 
         g.beta = 1.f;
         g.batch = batch;
         g.lower = 1;
-        cudaError_t e = launch_gemm_f32(g, s);
+        e = launch_gemm_f32(g, s);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
 
-cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int64_t n, float* C, int64_t ldc,
-                               int64_t strideC, int64_t m, int batch, cudaStream_t s) {
-    dim3 tg(static_cast<unsigned>((m + 127) / 128), batch);
+cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int64_t n, const float* Linv,
+                               int64_t strideL, float* C, int64_t ldc, int64_t strideC, int64_t m, int batch,
+                               cudaStream_t s) {
+    // Block row k of C times the inverse diagonal block (or its transpose), in place:
+    // every output column depends only on the same column of the block row.
+    auto diag = [&](int64_t k0, int nb, bool transpose) {
+        GemmArgs t{};
+        t.A = Linv + k0 * NB;
+        t.B = C + k0 * ldc;
+        t.C = C + k0 * ldc;
+        t.sam = transpose ? 1 : NB;
+        t.sak = transpose ? NB : 1;
+        t.sbk = ldc;
+        t.sbn = 1;
+        t.ldc = ldc;
+        t.strideA = strideL;
+        t.strideB = t.strideC = strideC;
+        t.M = nb;
+        t.N = m;
+        t.K = nb;
+        t.alpha = 1.f;
+        t.beta = 0.f;
+        t.batch = batch;
+        return launch_gemm_f32(t, s);
+    };
     // forward: L Y = C
     for (int64_t k0 = 0; k0 < n; k0 += NB) {
         const int nb = static_cast<int>(n - k0 < NB ? n - k0 : NB);
-        trsm_rhs_kernel<<<tg, 128, 0, s>>>(L, ldg, strideG, k0, nb, C, ldc, strideC, m, 0);
+        cudaError_t e = diag(k0, nb, false);
+        if (e != cudaSuccess) return e;
         const int64_t rem = n - k0 - nb;
         if (rem <= 0) continue;
         GemmArgs g{};
@@ -249,14 +388,15 @@ cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int
         g.alpha = -1.f;
         g.beta = 1.f;
         g.batch = batch;
-        cudaError_t e = launch_gemm_f32(g, s);
+        e = launch_gemm_f32(g, s);
         if (e != cudaSuccess) return e;
     }
     // backward: L^T X = Y
     const int64_t last = ((n - 1) / NB) * NB;
     for (int64_t k0 = last; k0 >= 0; k0 -= NB) {
         const int nb = static_cast<int>(n - k0 < NB ? n - k0 : NB);
-        trsm_rhs_kernel<<<tg, 128, 0, s>>>(L, ldg, strideG, k0, nb, C, ldc, strideC, m, 1);
+        cudaError_t e = diag(k0, nb, true);
+        if (e != cudaSuccess) return e;
         if (k0 == 0) break;
         GemmArgs g{};
         g.A = L + k0 * ldg;  // A(i, kk) = L[k0 + kk][i]
@@ -275,7 +415,7 @@ cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int
         g.alpha = -1.f;
         g.beta = 1.f;
         g.batch = batch;
-        cudaError_t e = launch_gemm_f32(g, s);
+        e = launch_gemm_f32(g, s);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

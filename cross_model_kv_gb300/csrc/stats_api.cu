@@ -48,6 +48,8 @@ struct kvb_stats {
     size_t wsD_bytes = 0;
     float* wsS = nullptr;
     size_t wsS_bytes = 0;
+    float* wsL = nullptr;  // inverses of the 64 x 64 diagonal blocks of the factors
+    size_t wsL_bytes = 0;
     float* r2 = nullptr;  // [2][L_t][L_s]
     int* sel = nullptr;   // [2][L_t][k]
     int* numeric = nullptr;
@@ -98,6 +100,7 @@ void free_stats(kvb_stats* st) {
     cudaFree(st->wsR);
     cudaFree(st->wsD);
     cudaFree(st->wsS);
+    cudaFree(st->wsL);
     if (st->plan) stats_gemm_tc_free(st->plan);
     delete st;
 }
@@ -417,6 +420,8 @@ kvb_status kvb_layer_select(kvb_ctx* c, kvb_stats* st, double lambda, int32_t* s
     if ((s = ws_grow(st, &st->wsR, &st->wsR_bytes, size_t(B) * q * Ft * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsD, &st->wsD_bytes, size_t(B) * q * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsS, &st->wsS_bytes, size_t(B) * Ft * 4)) != KVB_OK) return s;
+    const int64_t lq = ((q + 63) / 64) * 64 * 64;  // Linv floats per system
+    if ((s = ws_grow(st, &st->wsL, &st->wsL_bytes, size_t(B) * lq * 4)) != KVB_OK) return s;
     cudaError_t e = cudaMemsetAsync(st->numeric, 0, sizeof(int), cs);
     const float lam = static_cast<float>(lambda);
     {
@@ -430,9 +435,11 @@ kvb_status kvb_layer_select(kvb_ctx* c, kvb_stats* st, double lambda, int32_t* s
                 e = launch_gather_system(st->gram[kv], st->Fs, L, q, q, lam, st->wsG, int64_t(q) * q, st->wsD, nb, cs);
                 if (e == cudaSuccess)
                     e = launch_gather_rhs(st->cross[kv], Ft, L, q, q, Ft, st->wsD, st->wsR, int64_t(q) * Ft, nb, cs);
-                if (e == cudaSuccess) e = chol_factor_batched(st->wsG, q, int64_t(q) * q, q, nb, st->numeric, cs);
                 if (e == cudaSuccess)
-                    e = chol_solve_batched(st->wsG, q, int64_t(q) * q, q, st->wsR, Ft, int64_t(q) * Ft, Ft, nb, cs);
+                    e = chol_factor_batched(st->wsG, q, int64_t(q) * q, q, nb, st->numeric, st->wsL, lq, cs);
+                if (e == cudaSuccess)
+                    e = chol_solve_batched(st->wsG, q, int64_t(q) * q, q, st->wsL, lq, st->wsR, Ft, int64_t(q) * Ft, Ft,
+                                           nb, cs);
                 if (e == cudaSuccess)
                     e = launch_sse(st->cross[kv], Ft, L, q, q, Ft, st->wsD, st->wsR, int64_t(q) * Ft, st->syy[kv], lam,
                                    st->wsS, nb, cs);
@@ -484,6 +491,8 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
     if ((s = ws_grow(st, &st->wsG, &st->wsG_bytes, size_t(B) * p * p * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsR, &st->wsR_bytes, size_t(B) * p * q * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsD, &st->wsD_bytes, size_t(B) * p * 4)) != KVB_OK) return s;
+    const int64_t lp = ((p + 63) / 64) * 64 * 64;  // Linv floats per system
+    if ((s = ws_grow(st, &st->wsL, &st->wsL_bytes, size_t(B) * lp * 4)) != KVB_OK) return s;
     cudaError_t e = cudaMemsetAsync(st->numeric, 0, sizeof(int), cs);
     const float lam = static_cast<float>(lambda);
     void* Wout[2] = {W_k, W_v};
@@ -507,8 +516,9 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
                 }
                 e = launch_gather_system(st->gram[kv], st->Fs, L, q, p, lam, st->wsG, p * p, st->wsD, nb, cs);
                 if (e == cudaSuccess) e = launch_gather_rhs(st->cross[kv], st->Ft, L, q, p, q, st->wsD, st->wsR, p * q, nb, cs);
-                if (e == cudaSuccess) e = chol_factor_batched(st->wsG, p, p * p, p, nb, st->numeric, cs);
-                if (e == cudaSuccess) e = chol_solve_batched(st->wsG, p, p * p, p, st->wsR, q, p * q, q, nb, cs);
+                if (e == cudaSuccess) e = chol_factor_batched(st->wsG, p, p * p, p, nb, st->numeric, st->wsL, lp, cs);
+                if (e == cudaSuccess)
+                    e = chol_solve_batched(st->wsG, p, p * p, p, st->wsL, lp, st->wsR, q, p * q, q, nb, cs);
                 if (e == cudaSuccess) e = launch_write_w(w_dtype, st->wsR, p * q, st->wsD, p, q, O, nb, cs);
                 if (e == cudaSuccess)
                     e = launch_bias(st->wsR, p * q, st->wsD, p, q, L, q, st->mean[kv], st->mean[2 + kv], O, nb, cs);

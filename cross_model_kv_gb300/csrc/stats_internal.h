@@ -97,12 +97,15 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm_f32(const GemmArgs& g, cudaStream_t s);
 
-// In-place Cholesky of batch SPD matrices (lower triangle used), then in-place
-// solve of G X = C for m right-hand sides.  A non-positive pivot records
-// DEV_ERR_NUMERIC in *numeric_flag.
+// In-place blocked Cholesky of batch SPD matrices (lower triangle used; 64-wide
+// panels), then in-place solve of G X = C for m right-hand sides.  The factor
+// also leaves the inverse of every 64 x 64 diagonal block in Linv
+// ([batch][n/64 * 64][64], strideL floats per system), so both triangular
+// solves run as GEMMs.  A non-positive pivot sets *numeric_flag.
 cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t n, int batch, int* numeric_flag,
-                                cudaStream_t s);
-cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int64_t n, float* C, int64_t ldc,
-                               int64_t strideC, int64_t m, int batch, cudaStream_t s);
+                                float* Linv, int64_t strideL, cudaStream_t s);
+cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int64_t n, const float* Linv,
+                               int64_t strideL, float* C, int64_t ldc, int64_t strideC, int64_t m, int batch,
+                               cudaStream_t s);
 
 }  // namespace kvb

@@ -120,6 +120,23 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+# --------------------------------------------------------------------------- multi-rank helpers
+
+def max_over_ranks(value_ms: float, dist, device) -> float:
+    """Largest per-rank time: a job of independent replicas is as slow as its slowest rank."""
+    if dist is None:
+        return value_ms
+    import torch
+    t = torch.tensor([value_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, steps: int, world: int, total_ms: float) -> float:
+    """Whole-job mapped tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (total_ms / 1000.0)
+
+
 # --------------------------------------------------------------------------- oracle (CPU)
 
 def oracle_rate(src_k, src_v, pos, sel_k, sel_v, Wk, bk, Wv, bv, layers):
@@ -351,13 +368,9 @@ def run_gpu(args, rank, world, local_rank):
     kvb.kvb_profile_enable(ctx, False)
     kernels = kvb.kvb_profile_read(ctx)
     kvb.kvb_ctx_check(ctx, stream)
-    total_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms / 1000.0)
+    value = job_throughput(T, args.steps, world, total_ms)
     launches = sum(n for n, _ in kernels.values())
 
     if args.skip_extras:
@@ -427,12 +440,8 @@ def run_gpu(args, rank, world, local_rank):
     run_e2e(e2e_steps, e0)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * T * e2e_steps / (e2e_ms / 1000.0)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    e2e_value = job_throughput(T, e2e_steps, world, e2e_ms)
     kvb.kvb_ctx_check(ctx, stream)
     del h_src_k, h_src_v, h_out_k, h_out_v, bufs
 

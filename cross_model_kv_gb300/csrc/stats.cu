@@ -240,8 +240,8 @@ __global__ void __launch_bounds__(256, (R <= 4 ? 2 : 1)) gather_shift_kernel(con
                                                            void* __restrict__ out_lo, int64_t ld) {
     extern __shared__ float tile[];  // [d][kChunk + 1] then [rps][d] partial sums
     constexpr int LT = kChunk + 1;
-    const int slab = blockIdx.x;
-    const int chunk = blockIdx.y;
+    const int slab = blockIdx.y;  // chunks of one slab run side by side: contiguous reads and writes
+    const int chunk = blockIdx.x;
     const int r0 = chunk * kChunk;
     const int n = *nb;
     if (r0 >= ((n + kChunk - 1) / kChunk) * kChunk) return;
@@ -525,7 +525,7 @@ cudaError_t launch_gather(const GatherArgs& g, cudaStream_t s) {
         const int rps = 256 / (g.d >> 4);
         const int R = rps >= kChunk ? 1 : kChunk / rps;
         const size_t smem = (static_cast<size_t>(g.d) * (kChunk + 1) + static_cast<size_t>(rps) * g.d) * sizeof(float);
-        dim3 cgrid(static_cast<unsigned>(g.n_slabs), static_cast<unsigned>((g.T + kChunk - 1) / kChunk));
+        dim3 cgrid(static_cast<unsigned>((g.T + kChunk - 1) / kChunk), static_cast<unsigned>(g.n_slabs));
         const __nv_bfloat16* c16 = static_cast<const __nv_bfloat16*>(g.cache);
 #define KVB_GATHER(RR)                                                                                          \
     do {                                                                                                        \

@@ -40,9 +40,9 @@ Conventions (readings where the pages leave a step open):
   the lower source index; the k selected layers are returned ascending.
 
 Parity pins (tests/test_oracle_pins.py): rope, recode, ridge, centered_stats,
-chan_merge, single_source_r2, select_top_k, map_apply, fit_mapper and the size
-formulas are all pinned.  `synthesize_pair` builds test inputs and is checked
-only through the recovery pins.
+chan_merge, single_source_r2, select_top_k, map_apply, fit_mapper, the size
+formulas and the attention-output cosine are all pinned.  `synthesize_pair`
+builds test inputs and is checked only through the recovery pins.
 """
 from __future__ import annotations
 
@@ -57,7 +57,8 @@ __all__ = [
     "ridge_from_stats", "fit_ridge", "single_source_r2", "select_top_k",
     "map_apply", "fit_mapper", "FitResult", "retain_stride",
     "synthesize_pair", "head_pooled_r2", "mapper_param_count",
-    "fit_stats_bytes", "stride_observations",
+    "fit_stats_bytes", "stride_observations", "attention_output",
+    "attention_cosine",
 ]
 
 
@@ -426,3 +427,57 @@ def fit_stats_bytes(k: int, H: int, d: int, layers_per_block: int = 1, itemsize:
 def stride_observations(n_sequences: int, seq_len: int, stride: int) -> int:
     """Observations kept from n_sequences x seq_len tokens with positions 0..seq_len-1."""
     return n_sequences * int(np.sum(retain_stride(np.arange(seq_len), stride)))
+
+
+# ---------------------------------------------------------------------------
+# Attention-output cosine (quality diagnostic)
+# KVBridge "Real-model T2 evidence": the gate is on the mean and the minimum
+# of the attention-output cosine; KVBridge "Scope and limitations" and Velox
+# "The honesty crux" item 6: this cosine, not the calibration R^2, tracks
+# downstream retention; Velox "What is not implemented" lists it as the
+# screen to run on a pair before deploying it.
+# ---------------------------------------------------------------------------
+
+def attention_output(q, q_pos, k, v, kv_pos) -> np.ndarray:
+    """o[l][hq][i] = sum over visible j of softmax_j(q_i . k_j / sqrt(d)) v_j.
+
+    q is [L][Hq][Tq][d] (post-RoPE target queries), k and v are [L][H][T][d]
+    (post-RoPE keys, as caches store them).  Query head hq reads KV head
+    hq // (Hq / H) (grouped-query attention).  Key j is visible to query i
+    iff kv_pos[j] <= q_pos[i] (causal by position within one sequence).  A
+    query with no visible key gets the zero vector.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    L, Hq, Tq, d = q.shape
+    H = k.shape[1]
+    if Hq % H:
+        raise ValueError("query heads must be a multiple of the KV heads")
+    g = Hq // H
+    visible = np.asarray(kv_pos)[None, :] <= np.asarray(q_pos)[:, None]   # [Tq][T]
+    out = np.zeros((L, Hq, Tq, d))
+    for l in range(L):
+        for hq in range(Hq):
+            kh = hq // g
+            scores = q[l, hq] @ k[l, kh].T / np.sqrt(d)
+            for i in range(Tq):
+                if not visible[i].any():
+                    continue
+                s = scores[i][visible[i]]
+                w = np.exp(s - s.max())
+                out[l, hq, i] = (w / w.sum()) @ v[l, kh][visible[i]]
+    return out
+
+
+def attention_cosine(q, q_pos, k_a, v_a, k_b, v_b, kv_pos) -> np.ndarray:
+    """cos(o_a, o_b) per [L][Hq][Tq] row, o_x = attention_output with cache x.
+
+    Cache a is the one under test (the mapped cache), cache b the reference
+    (the target's own prefill).  The cosine is 0 where either output is zero.
+    """
+    oa = attention_output(q, q_pos, k_a, v_a, kv_pos)
+    ob = attention_output(q, q_pos, k_b, v_b, kv_pos)
+    dot = (oa * ob).sum(axis=-1)
+    den = np.sqrt((oa * oa).sum(axis=-1)) * np.sqrt((ob * ob).sum(axis=-1))
+    return np.where(den > 0, dot / np.where(den > 0, den, 1.0), 0.0)

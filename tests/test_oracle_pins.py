@@ -445,3 +445,76 @@ def test_sizes_match_the_pages(golden_dir):
     pair = _tiny_pair(5, n_seq=1)
     fit = O.fit_mapper(pair["calib"], 1e4, 5e4, 2, 0.01, 4)
     assert fit.W_k.size + fit.W_v.size + fit.b_k.size + fit.b_v.size == O.mapper_param_count(6, 2, 2, 16)
+
+
+# --------------------------------------------------------------------------
+# Attention-output cosine
+# --------------------------------------------------------------------------
+
+def _attn_inputs(seed, L=2, H=2, g=3, T=37, d=16):
+    q = synth.content(seed, L, H * g, T, d, 0.5)
+    k = synth.content(seed + 1, L, H, T, d, 0.5)
+    v = synth.content(seed + 2, L, H, T, d, 0.5)
+    return q, k, v
+
+
+def test_attention_output_matches_torch_sdpa_causal_gqa():
+    # library route: scaled_dot_product_attention (default scale 1/sqrt(d),
+    # is_causal) with each KV head repeated for its group of query heads
+    torch = pytest.importorskip("torch")
+    q, k, v = _attn_inputs(70)
+    g = q.shape[1] // k.shape[1]
+    pos = np.arange(q.shape[2])
+    o = O.attention_output(q, pos, k, v, pos)
+    kt = torch.from_numpy(k).repeat_interleave(g, dim=1)
+    vt = torch.from_numpy(v).repeat_interleave(g, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q), kt, vt, is_causal=True)
+    assert np.abs(o - ref.numpy()).max() < 1e-12
+
+
+def test_attention_output_subset_queries_equal_rows_of_the_full_result():
+    q, k, v = _attn_inputs(71)
+    pos = np.arange(q.shape[2]) + 100
+    full = O.attention_output(q, pos, k, v, pos)
+    rows = np.array([0, 5, 36])
+    part = O.attention_output(q[:, :, rows], pos[rows], k, v, pos)
+    assert np.abs(part - full[:, :, rows]).max() < 1e-13
+
+
+def test_attention_output_first_position_sees_only_the_first_key():
+    q, k, v = _attn_inputs(72)
+    g = q.shape[1] // k.shape[1]
+    pos = np.arange(q.shape[2])
+    o = O.attention_output(q[:, :, :1], pos[:1], k, v, pos)
+    for hq in range(q.shape[1]):
+        assert np.array_equal(o[:, hq, 0], v[:, hq // g, 0])
+
+
+def test_attention_output_query_with_no_visible_key_is_zero():
+    q, k, v = _attn_inputs(73)
+    o = O.attention_output(q[:, :, :2], np.array([-1, 0]), k, v, np.arange(q.shape[2]))
+    assert np.all(o[:, :, 0] == 0) and np.all(o[:, :, 1] != 0)
+
+
+def test_attention_cosine_invariants():
+    q, k, v = _attn_inputs(74)
+    pos = np.arange(q.shape[2])
+    one = O.attention_cosine(q, pos, k, v, k, v, pos)
+    assert np.abs(one - 1).max() < 1e-12
+    # scaling the values scales every output: +1 for c > 0, -1 for c < 0
+    assert np.abs(O.attention_cosine(q, pos, k, v, k, 2.5 * v, pos) - 1).max() < 1e-12
+    assert np.abs(O.attention_cosine(q, pos, k, v, k, -0.5 * v, pos) + 1).max() < 1e-12
+    # one vector added to every key of a head shifts each query's scores by a
+    # constant: softmax, hence the output, is unchanged
+    u = synth.content(75, k.shape[0], k.shape[1], 1, k.shape[3], 0.0)
+    assert np.abs(O.attention_cosine(q, pos, k, v, k + u, v, pos) - 1).max() < 1e-10
+    # a perturbed cache gives a cosine strictly inside (-1, 1), equal to the
+    # library cosine of the two outputs
+    torch = pytest.importorskip("torch")
+    k2 = k + 0.5 * synth.noise(76, k.shape)
+    v2 = v + 0.5 * synth.noise(77, v.shape)
+    c = O.attention_cosine(q, pos, k2, v2, k, v, pos)
+    oa = torch.from_numpy(O.attention_output(q, pos, k2, v2, pos))
+    ob = torch.from_numpy(O.attention_output(q, pos, k, v, pos))
+    assert np.abs(c - torch.nn.functional.cosine_similarity(oa, ob, dim=-1).numpy()).max() < 1e-12
+    assert c.max() < 1 and c.min() > -1 and c.mean() > 0.5

@@ -307,6 +307,89 @@ def run_fit(kvb, dev, seed=101, small=False):
     return out
 
 
+ATTN = dict(L=64, H=8, Hq=64, d=128, n_seq=8, seq_len=256, noise=0.3)
+
+
+def run_attention(kvb, dev, seed=301):
+    """Attention-output cosine diagnostic, Qwen3-32B target geometry.
+
+    Eight held-out sequences of 256 tokens, every position a query (causal),
+    64 layers x 64 query heads over 8 KV heads, head_dim 128, bf16: one
+    kvb_attention_cosine call per sequence.  Cache a = cache b + noise (the
+    values do not change the work).  Algorithmic flops count only the visible
+    (query, key) pairs: 4 d flops each (scores and weighted values) per cache.
+    """
+    import torch
+    import synth
+
+    A = ATTN
+    L, H, Hq, d, T = A["L"], A["H"], A["Hq"], A["d"], A["seq_len"]
+    spec = lambda n: {"n_layers": n, "n_kv_heads": H, "head_dim": d, "rope_theta": 1e6}
+    ctx = kvb.kvb_ctx_create(spec(1), spec(L), 1, T, dev.index or 0)
+    seqs = []
+    for i in range(A["n_seq"]):
+        q = synth.torch_content(seed + 10 * i, L, Hq, T, d, 0.5, torch.bfloat16, dev)
+        kb = synth.torch_content(seed + 10 * i + 1, L, H, T, d, 0.5, torch.bfloat16, dev)
+        vb = synth.torch_content(seed + 10 * i + 2, L, H, T, d, 0.5, torch.bfloat16, dev)
+        ka = (kb.float() + A["noise"] * synth.torch_content(seed + 10 * i + 3, L, H, T, d, 0.0, torch.float32, dev)
+              ).to(torch.bfloat16)
+        va = (vb.float() + A["noise"] * synth.torch_content(seed + 10 * i + 4, L, H, T, d, 0.0, torch.float32, dev)
+              ).to(torch.bfloat16)
+        seqs.append((q, ka, va, kb, vb))
+    pos = torch.arange(T, dtype=torch.int32, device=dev)
+    out = torch.empty((A["n_seq"], L, Hq, T), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for i, (q, ka, va, kb, vb) in enumerate(seqs):
+            kvb.kvb_attention_cosine(ctx, q, pos, ka, va, kb, vb, pos, out[i], stream)
+
+    step()
+    torch.cuda.synchronize(dev)
+    kvb.kvb_profile_read(ctx)
+    kvb.kvb_profile_enable(ctx, True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 3
+    e0.record(stream)
+    for _ in range(reps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    kvb.kvb_profile_enable(ctx, False)
+    kvb.kvb_ctx_check(ctx, stream)
+    ms = e0.elapsed_time(e1) / reps
+    n, kern_ms = kvb.kvb_profile_read(ctx).get("attention_cosine", (0, 0.0))
+    flop = A["n_seq"] * (T * (T + 1) // 2) * L * Hq * 4 * d * 2
+    cos = out.double()
+    res = {"workload": f"qwen3-32b target geometry ({L} layers, {Hq} query / {H} KV heads, d={d}): "
+                       f"{A['n_seq']} held-out sequences x {T} tokens, all positions queried, bf16 caches",
+           "ms_per_pass": ms, "kernel": "attention_cosine", "launches_per_pass": n // reps,
+           "avg_launch_ms": kern_ms / max(n, 1), "algorithmic_flop_per_pass": flop,
+           "achieved_tflops": flop / (kern_ms / reps / 1e3) / 1e12 if kern_ms else None,
+           "cos_mean": float(cos.mean()), "cos_min": float(cos.min()),
+           "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count}
+    del seqs, out
+    kvb.kvb_ctx_destroy(ctx)
+    torch.cuda.empty_cache()
+    return res
+
+
+def attn_roofline(attn, clk):
+    """Roofline of the attention-cosine kernel: fp32 FMA on CUDA cores.
+
+    Peak = SMs x 128 fp32 lanes x 2 flop x the maximum SM clock that the
+    sampler read (2070 MHz when it read none).
+    """
+    if attn is None:
+        return None
+    mhz = (clk or {}).get("sm_max_mhz") or 2070.0
+    peak = attn["sm_count"] * 128 * 2 * mhz * 1e6 / 1e12
+    a = attn.get("achieved_tflops")
+    return dict(attn, roofline={"bound": "alu", "achieved": a, "peak": peak, "unit": "TFLOP/s",
+                                "frac": a / peak if a else None,
+                                "peak_kind": f"derived: {attn['sm_count']} SMs x 128 fp32 lanes x 2 flop x {mhz:.0f} MHz"})
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args, rank, world, local_rank):
@@ -462,6 +545,9 @@ def run_gpu(args, rank, world, local_rank):
     fit = None
     if not args.skip_fit:
         fit = run_fit(kvb, dev)
+    attn = None
+    if not args.skip_attn:
+        attn = run_attention(kvb, dev)
 
     if rank != 0:
         return
@@ -505,6 +591,7 @@ def run_gpu(args, rank, world, local_rank):
                        "positions and D2H of target K/V; steps pipelined on copy/compute streams with "
                        "double-buffered device buffers"},
         "fit": fit,
+        "attention_cosine": attn_roofline(attn, clk),
         "cpu_baseline": {"value": cpu_rate, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
                          "sample": f"{n_l} of {L_t} target layers x {T_cpu} tokens, float64, scaled to a full map",
                          "seconds": cpu_s},
@@ -522,6 +609,8 @@ def main():
                     help="small: T=4096 with the same layer shapes (for profiler captures)")
     ap.add_argument("--skip-extras", action="store_true", help="skip the end-to-end, fit and CPU-baseline legs")
     ap.add_argument("--skip-fit", action="store_true", help="skip the calibration-statistics / fit leg")
+    ap.add_argument("--skip-attn", action="store_true", help="skip the attention-output cosine leg")
+    ap.add_argument("--attn-only", action="store_true", help="run only the attention-output cosine leg")
     ap.add_argument("--fit-only", action="store_true", help="run only the fit leg (with --workload small: 8 -> 8 layers)")
     args = ap.parse_args()
     if args.workload == "small":
@@ -534,16 +623,19 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank)
         return
-    if args.fit_only:
+    if args.fit_only or args.attn_only:
         import torch
         from cross_model_kv_gb300 import build as kbuild
         kbuild.build()
         import cross_model_kv_gb300 as kvb
         dev = torch.device("cuda", local_rank)
         torch.cuda.set_device(dev)
-        fit = run_fit(kvb, dev, small=args.workload == "small")
+        if args.attn_only:
+            res = {"attention_cosine": attn_roofline(run_attention(kvb, dev), None)}
+        else:
+            res = {"fit": run_fit(kvb, dev, small=args.workload == "small")}
         if rank == 0:
-            print(json.dumps({"fit": fit}), flush=True)
+            print(json.dumps(res), flush=True)
         return
     if world > 1:
         import torch

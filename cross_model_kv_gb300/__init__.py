@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     KvbError,
     SIGNATURES,
     Stats,
+    kvb_attention_cosine,
     kvb_ctx_check,
     kvb_ctx_create,
     kvb_ctx_destroy,

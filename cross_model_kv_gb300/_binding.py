@@ -70,6 +70,8 @@ SIGNATURES = {
     "kvb_stats_import": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P, _P, _P]),
     "kvb_layer_select": (ctypes.c_int, [_P, _P, ctypes.c_double, _I32P, _I32P, _P, _P]),
     "kvb_ridge_solve": (ctypes.c_int, [_P, _P, _I32P, _I32P, ctypes.c_double, ctypes.c_int, _P, _P, _P, _P, _P]),
+    "kvb_attention_cosine": (ctypes.c_int, [_P, ctypes.c_int, _P, ctypes.c_int32, _P, ctypes.c_int64, _P, _P, _P,
+                                            _P, _P, ctypes.c_int64, _P, _P]),
 }
 
 _lib = None
@@ -306,3 +308,15 @@ def kvb_ridge_solve(ctx: Ctx, st: Stats, sel_k, sel_v, lam, W_k, W_v, b_k, b_v, 
     _check(load_library().kvb_ridge_solve(ctx.handle, st.handle, sk.ctypes.data_as(_I32P),
                                           sv.ctypes.data_as(_I32P), float(lam), _dtype_of(W_k), _dev(W_k),
                                           _dev(W_v), _dev(b_k), _dev(b_v), _stream(stream)))
+
+
+def kvb_attention_cosine(ctx: Ctx, q, q_pos, k_a, v_a, k_b, v_b, kv_pos, cos_out, stream=None):
+    """cos_out [L_t][Hq][Tq] = cosine of the attention outputs with caches a and b.
+
+    q [L_t][Hq][Tq][d], caches [L_t][H][T][d] (same dtype), q_pos int32 [Tq]
+    and kv_pos int32 [T] on the device; key j is visible to query i iff
+    kv_pos[j] <= q_pos[i].
+    """
+    _check(load_library().kvb_attention_cosine(
+        ctx.handle, _dtype_of(q), _dev(q), int(q.shape[1]), _dev(q_pos), int(q.shape[2]), _dev(k_a), _dev(v_a),
+        _dev(k_b), _dev(v_b), _dev(kv_pos), int(k_a.shape[2]), _dev(cos_out), _stream(stream)))

@@ -242,6 +242,33 @@ kvb_status kvb_ridge_solve(kvb_ctx* ctx, kvb_stats* st, const int32_t* sel_k_hos
                            const int32_t* sel_v_host, double lambda, kvb_dtype w_dtype, void* W_k,
                            void* W_v, float* b_k, float* b_v, void* stream);
 
+/*
+ * Attention-output cosine, a quality diagnostic for a mapped cache ("KVBridge"
+ * README, "Real-model T2 evidence": gate on its mean and minimum; "Scope and
+ * limitations", and "Cross-Model KV Transfer", "The honesty crux" item 6: it
+ * tracks downstream retention where the calibration R^2 does not).  For every
+ * target layer l, query head hq and query i:
+ *     o_x = sum over visible j of softmax_j(q_i . k_x[j] / sqrt(d)) v_x[j]
+ * for cache x in {a, b}, and cos_out[l][hq][i] = o_a . o_b / (|o_a| |o_b|)
+ * (0 where either output is zero).  Query head hq reads KV head
+ * hq / (n_q_heads / H) (grouped-query attention); key j is visible to query
+ * i iff kv_pos[j] <= q_pos[i], so one call covers one sequence.
+ *   q        device [L_tgt][n_q_heads][Tq][d] in dtype (post-RoPE queries)
+ *   q_pos    device int32 [Tq]
+ *   k_a, v_a device [L_tgt][H][T][d] in dtype: the cache under test
+ *   k_b, v_b device, same shape: the reference cache
+ *   kv_pos   device int32 [T]
+ *   cos_out  device float32 [L_tgt][n_q_heads][Tq], written in full
+ * Geometry (L_tgt, H, d) comes from the context's target model; d must be
+ * 16, 32, 64 or 128 and n_q_heads a multiple of H.  With T = 0 the cache
+ * pointers may be NULL and every cosine is 0; with Tq = 0 nothing is read.
+ * fp32 arithmetic throughout.  Asynchronous on `stream`.
+ */
+kvb_status kvb_attention_cosine(kvb_ctx* ctx, kvb_dtype dtype, const void* q, int32_t n_q_heads,
+                                const int32_t* q_pos, int64_t Tq, const void* k_a, const void* v_a,
+                                const void* k_b, const void* v_b, const int32_t* kv_pos, int64_t T,
+                                float* cos_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -11,6 +11,11 @@ import synth
 TOL_F32 = 1e-4
 TOL_BF16 = 1e-2
 TOL_W = 1e-3
+# Attention-output cosine: absolute error per row.  fp32 dot products of
+# length d <= 128 and softmax sums over a few thousand keys carry relative
+# errors near 1e-6 (plus the fast exponential's ~2^-21); a cosine moves by at
+# most the relative error of its two outputs, so 1e-4 leaves a wide margin.
+TOL_COS = 1e-4
 
 
 def rel_fro(a, b) -> float:

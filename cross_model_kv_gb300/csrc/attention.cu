@@ -11,8 +11,9 @@
 // (query head hq reads KV head hq / (H_q / H)).  Keys stream through shared
 // memory 32 at a time with an online softmax; the first cache's outputs stay
 // in registers while the second cache streams, then each row's cosine is
-// written.  Four threads per row, each scoring every fourth key and owning a
-// quarter of the output dims.  Causal by position: key j is attended by
+// written.  Eight threads share two query rows: each scores every eighth key
+// of the tile for both rows and owns every eighth float4 column of both
+// outputs (a 2 x 4 register tile per step).  Causal by position: key j is attended by
 // query i iff kv_pos[j] <= q_pos[i].  fp32 arithmetic on CUDA cores: the
 // diagnostic runs on a few held-out sequences, not on the transfer path.
 #include <climits>
@@ -23,10 +24,10 @@ namespace kvb {
 
 namespace {
 
-constexpr int KT = 32;    // keys per shared-memory tile
-constexpr int TPR = 4;    // threads per query row
-constexpr int NT = 256;   // threads per CTA
-constexpr int RMAX = NT / TPR;  // query rows per CTA
+constexpr int KT = 32;          // keys per shared-memory tile
+constexpr int NT = 256;         // threads per CTA
+constexpr int GRP = 8;          // threads per group; a group owns two query rows
+constexpr int RMAX = 2 * NT / GRP;  // query rows per CTA (64)
 
 struct AttnParams {
     const void* q;      // [L][Hq][Tq][D]
@@ -56,23 +57,32 @@ __device__ __forceinline__ void load8(const float* p, float* o) {
     o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
     o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
-__device__ __forceinline__ void store8(float* s, const float* v) {
-    reinterpret_cast<float4*>(s)[0] = make_float4(v[0], v[1], v[2], v[3]);
-    reinterpret_cast<float4*>(s)[1] = make_float4(v[4], v[5], v[6], v[7]);
+// Store eight floats as two float4.  Thread i of an eight-thread phase writes
+// its halves in the order given by bit 2 of i, so that each phase touches
+// eight distinct 16-byte bank groups.
+__device__ __forceinline__ void store8(float* s, const float* v, int lane) {
+    const int h = (lane >> 2) & 1;
+    float4* d = reinterpret_cast<float4*>(s);
+    const float4 lo = make_float4(v[0], v[1], v[2], v[3]);
+    const float4 hi = make_float4(v[4], v[5], v[6], v[7]);
+    d[h] = h ? hi : lo;
+    d[h ^ 1] = h ? lo : hi;
 }
 
-// Shared-memory layout (floats): q [RMAX][D+4] | k [KT][D+4] | v [KT][D] | p [RMAX][KT+1].
+// Shared-memory layout (floats): q [RMAX][D+4] | k [KT][D+4] | v [KT][D] | p [RMAX][KT+4].
 // The +4 keeps rows float4-aligned while shifting consecutive rows by four banks.
 template <int D>
 constexpr size_t attn_smem_bytes() {
-    return (static_cast<size_t>(RMAX) * (D + 4) + KT * (D + 4) + KT * D + RMAX * (KT + 1)) * sizeof(float);
+    return (static_cast<size_t>(RMAX) * (D + 4) + KT * (D + 4) + KT * D + RMAX * (KT + 4)) * sizeof(float);
 }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(NT, 2) attn_cosine_kernel(const __grid_constant__ AttnParams P) {
     constexpr int QLD = D + 4;
-    constexpr int DQ = D / TPR;   // output dims per thread
-    constexpr int KQ = KT / TPR;  // keys per thread per tile
+    constexpr int PLD = KT + 4;
+    constexpr int DC = D / 4;                     // float4 columns of a row
+    constexpr int CPT = (DC + GRP - 1) / GRP;     // float4 columns per thread (ragged for D = 16)
+    constexpr int KPT = KT / GRP;                 // keys per thread per tile
     extern __shared__ float4 sm4[];
     float* qs = reinterpret_cast<float*>(sm4);
     float* ks = qs + RMAX * QLD;
@@ -80,6 +90,7 @@ __global__ void __launch_bounds__(NT, 2) attn_cosine_kernel(const __grid_constan
     float* ps = vs + KT * D;
     __shared__ int qpos_s[RMAX];
     __shared__ int kpos_s[KT];
+    __shared__ int qpos_max;
 
     const int g = P.Hq / P.H;
     const int rows = g * P.Tq;
@@ -87,11 +98,13 @@ __global__ void __launch_bounds__(NT, 2) attn_cosine_kernel(const __grid_constan
     const int l = blockIdx.y / P.H;
     const int kh = blockIdx.y % P.H;
     const int tid = threadIdx.x;
-    const int r = tid / TPR;    // local row
-    const int qd = tid % TPR;   // quarter: keys qd, qd+4, ...; float4 columns qd, qd+4, ...
-    const bool row_ok = r0 + r < rows;
+    const int lane = tid & 31;
+    const int grp = tid / GRP;     // rows 2 grp, 2 grp + 1
+    const int t = tid % GRP;       // keys t, t + 8, ...; float4 columns t, t + 8, ...
+    const int ra = 2 * grp;
 
     // the CTA's query rows: row gr is (query head kh*g + gr / Tq, query gr % Tq)
+    if (tid == 0) qpos_max = INT_MIN;
     const T* qbase = static_cast<const T*>(P.q);
     for (int e = tid; e < RMAX * (D / 8); e += NT) {
         const int rr = e / (D / 8), c8 = (e % (D / 8)) * 8;
@@ -101,31 +114,29 @@ __global__ void __launch_bounds__(NT, 2) attn_cosine_kernel(const __grid_constan
             const int hh = kh * g + grr / P.Tq, ii = grr % P.Tq;
             load8(qbase + ((static_cast<int64_t>(l) * P.Hq + hh) * P.Tq + ii) * D + c8, v);
         }
-        store8(qs + rr * QLD + c8, v);
+        store8(qs + rr * QLD + c8, v, lane);
     }
-    __shared__ int qpos_max;
-    if (tid == 0) qpos_max = INT_MIN;
     __syncthreads();
     for (int e = tid; e < RMAX; e += NT) {
         const int grr = r0 + e;
-        qpos_s[e] = grr < rows ? P.q_pos[grr % P.Tq] : -1;
+        qpos_s[e] = grr < rows ? P.q_pos[grr % P.Tq] : INT_MIN;
         if (grr < rows) atomicMax(&qpos_max, qpos_s[e]);
     }
     __syncthreads();
-    const int my_qpos = qpos_s[r];
+    const int qpos0 = qpos_s[ra], qpos1 = qpos_s[ra + 1];
     const int cta_qpos = qpos_max;
 
-    float oa[DQ];
-    float na = 0.f, nb = 0.f, dot = 0.f;
+    float oa[2][4 * CPT];
+    float na[2] = {0.f, 0.f}, nb[2] = {0.f, 0.f}, dot[2] = {0.f, 0.f};
 #pragma unroll 1
     for (int which = 0; which < 2; ++which) {
         const int64_t head = (static_cast<int64_t>(l) * P.H + kh) * P.T * D;
         const T* K = static_cast<const T*>(P.k[which]) + head;
         const T* V = static_cast<const T*>(P.v[which]) + head;
-        float acc[DQ];
+        float acc[2][4 * CPT];
 #pragma unroll
-        for (int c = 0; c < DQ; ++c) acc[c] = 0.f;
-        float m = -INFINITY, lsum = 0.f;
+        for (int c = 0; c < 4 * CPT; ++c) acc[0][c] = acc[1][c] = 0.f;
+        float m[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
 #pragma unroll 1
         for (int64_t j0 = 0; j0 < P.T; j0 += KT) {
             // skip a tile none of whose keys any row of the CTA may see (the
@@ -141,93 +152,114 @@ __global__ void __launch_bounds__(NT, 2) attn_cosine_kernel(const __grid_constan
                     load8(K + (j0 + jj) * D + c8, kv8);
                     load8(V + (j0 + jj) * D + c8, vv8);
                 }
-                store8(ks + jj * QLD + c8, kv8);
-                store8(vs + jj * D + c8, vv8);
+                store8(ks + jj * QLD + c8, kv8, lane);
+                store8(vs + jj * D + c8, vv8, lane);
             }
-            for (int e = tid; e < KT; e += NT) kpos_s[e] = j0 + e < P.T ? P.kv_pos[j0 + e] : 0;
+            if (tid < KT) kpos_s[tid] = j0 + tid < P.T ? P.kv_pos[j0 + tid] : 0;
             __syncthreads();
 
-            // scores of keys qd, qd + 4, ... of the tile
-            float s[KQ];
-            float tmax = -INFINITY;
-            const float4* qr = reinterpret_cast<const float4*>(qs + r * QLD);
+            // scores: 2 rows x KPT keys per thread, one float4 of q and k per step
+            float s[2][KPT];
 #pragma unroll
-            for (int jj = 0; jj < KQ; ++jj) {
-                const int j = jj * TPR + qd;
-                const float4* kr = reinterpret_cast<const float4*>(ks + j * QLD);
-                float a0 = 0.f, a1 = 0.f;
-#pragma unroll 8
-                for (int c = 0; c < D / 4; ++c) {
-                    const float4 x = qr[c], y = kr[c];
-                    a0 = fmaf(x.x, y.x, a0);
-                    a1 = fmaf(x.y, y.y, a1);
-                    a0 = fmaf(x.z, y.z, a0);
-                    a1 = fmaf(x.w, y.w, a1);
+            for (int i = 0; i < KPT; ++i) s[0][i] = s[1][i] = 0.f;
+            const float4* q0 = reinterpret_cast<const float4*>(qs + ra * QLD);
+            const float4* q1 = reinterpret_cast<const float4*>(qs + (ra + 1) * QLD);
+#pragma unroll 1
+            for (int c = 0; c < DC; ++c) {
+                const float4 x0 = q0[c], x1 = q1[c];
+#pragma unroll
+                for (int i = 0; i < KPT; ++i) {
+                    const float4 y = reinterpret_cast<const float4*>(ks + (t + GRP * i) * QLD)[c];
+                    s[0][i] = fmaf(x0.x, y.x, fmaf(x0.y, y.y, fmaf(x0.z, y.z, fmaf(x0.w, y.w, s[0][i]))));
+                    s[1][i] = fmaf(x1.x, y.x, fmaf(x1.y, y.y, fmaf(x1.z, y.z, fmaf(x1.w, y.w, s[1][i]))));
                 }
-                const bool ok = row_ok && j0 + j < P.T && kpos_s[j] <= my_qpos;
-                s[jj] = ok ? (a0 + a1) * P.scale : -INFINITY;
-                tmax = fmaxf(tmax, s[jj]);
             }
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-            // online softmax: rescale what was accumulated to the new running max
-            const float mnew = fmaxf(m, tmax);
-            const float alpha = mnew == -INFINITY ? 1.f : __expf(m - mnew);
-            float psum = 0.f;
+            float alpha[2];
 #pragma unroll
-            for (int jj = 0; jj < KQ; ++jj) {
-                const float p = s[jj] == -INFINITY ? 0.f : __expf(s[jj] - mnew);
-                ps[r * (KT + 1) + jj * TPR + qd] = p;
-                psum += p;
+            for (int rr = 0; rr < 2; ++rr) {
+                const int qp = rr ? qpos1 : qpos0;
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < KPT; ++i) {
+                    const int j = t + GRP * i;
+                    const bool ok = j0 + j < P.T && kpos_s[j] <= qp;
+                    s[rr][i] = ok ? s[rr][i] * P.scale : -INFINITY;
+                    tmax = fmaxf(tmax, s[rr][i]);
+                }
+#pragma unroll
+                for (int o = 1; o < GRP; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+                // online softmax: rescale what was accumulated to the new running max
+                const float mnew = fmaxf(m[rr], tmax);
+                alpha[rr] = mnew == -INFINITY ? 1.f : __expf(m[rr] - mnew);
+                float psum = 0.f;
+#pragma unroll
+                for (int i = 0; i < KPT; ++i) {
+                    const float p = s[rr][i] == -INFINITY ? 0.f : __expf(s[rr][i] - mnew);
+                    ps[(ra + rr) * PLD + t + GRP * i] = p;
+                    psum += p;
+                }
+#pragma unroll
+                for (int o = 1; o < GRP; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+                lsum[rr] = lsum[rr] * alpha[rr] + psum;
+                m[rr] = mnew;
             }
-            psum += __shfl_xor_sync(0xffffffffu, psum, 1);
-            psum += __shfl_xor_sync(0xffffffffu, psum, 2);
-            lsum = lsum * alpha + psum;
-            m = mnew;
-            __syncwarp();  // the row's four threads are in one warp
+            __syncwarp();  // a group's eight threads are in one warp
 #pragma unroll
-            for (int c = 0; c < DQ; ++c) acc[c] *= alpha;
+            for (int c = 0; c < 4 * CPT; ++c) {
+                acc[0][c] *= alpha[0];
+                acc[1][c] *= alpha[1];
+            }
+            // weighted values: 2 rows x CPT float4 columns per thread
 #pragma unroll 4
             for (int j = 0; j < KT; ++j) {
-                const float p = ps[r * (KT + 1) + j];
+                const float p0 = ps[ra * PLD + j], p1 = ps[(ra + 1) * PLD + j];
                 const float4* vr = reinterpret_cast<const float4*>(vs + j * D);
 #pragma unroll
-                for (int c = 0; c < DQ / 4; ++c) {
-                    const float4 y = vr[c * TPR + qd];
-                    acc[4 * c] = fmaf(p, y.x, acc[4 * c]);
-                    acc[4 * c + 1] = fmaf(p, y.y, acc[4 * c + 1]);
-                    acc[4 * c + 2] = fmaf(p, y.z, acc[4 * c + 2]);
-                    acc[4 * c + 3] = fmaf(p, y.w, acc[4 * c + 3]);
+                for (int c = 0; c < CPT; ++c) {
+                    if (t + GRP * c < DC) {
+                        const float4 y = vr[t + GRP * c];
+                        acc[0][4 * c] = fmaf(p0, y.x, acc[0][4 * c]);
+                        acc[0][4 * c + 1] = fmaf(p0, y.y, acc[0][4 * c + 1]);
+                        acc[0][4 * c + 2] = fmaf(p0, y.z, acc[0][4 * c + 2]);
+                        acc[0][4 * c + 3] = fmaf(p0, y.w, acc[0][4 * c + 3]);
+                        acc[1][4 * c] = fmaf(p1, y.x, acc[1][4 * c]);
+                        acc[1][4 * c + 1] = fmaf(p1, y.y, acc[1][4 * c + 1]);
+                        acc[1][4 * c + 2] = fmaf(p1, y.z, acc[1][4 * c + 2]);
+                        acc[1][4 * c + 3] = fmaf(p1, y.w, acc[1][4 * c + 3]);
+                    }
                 }
             }
         }
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-        if (which == 0) {
 #pragma unroll
-            for (int c = 0; c < DQ; ++c) {
-                oa[c] = acc[c] * inv;
-                na = fmaf(oa[c], oa[c], na);
-            }
-        } else {
+        for (int rr = 0; rr < 2; ++rr) {
+            const float inv = lsum[rr] > 0.f ? 1.f / lsum[rr] : 0.f;
 #pragma unroll
-            for (int c = 0; c < DQ; ++c) {
-                const float ob = acc[c] * inv;
-                dot = fmaf(oa[c], ob, dot);
-                nb = fmaf(ob, ob, nb);
+            for (int c = 0; c < 4 * CPT; ++c) {
+                const float o = acc[rr][c] * inv;  // columns a thread does not own stay 0
+                if (which == 0) {
+                    oa[rr][c] = o;
+                    na[rr] = fmaf(o, o, na[rr]);
+                } else {
+                    dot[rr] = fmaf(oa[rr][c], o, dot[rr]);
+                    nb[rr] = fmaf(o, o, nb[rr]);
+                }
             }
         }
     }
 #pragma unroll
-    for (int o = 1; o < TPR; o <<= 1) {
-        dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        na += __shfl_xor_sync(0xffffffffu, na, o);
-        nb += __shfl_xor_sync(0xffffffffu, nb, o);
-    }
-    if (row_ok && qd == 0) {
-        const int gr = r0 + r;
-        const int hq = kh * g + gr / P.Tq, qi = gr % P.Tq;
-        const float den = sqrtf(na) * sqrtf(nb);
-        P.cos_out[(static_cast<int64_t>(l) * P.Hq + hq) * P.Tq + qi] = den > 0.f ? dot / den : 0.f;
+    for (int rr = 0; rr < 2; ++rr) {
+#pragma unroll
+        for (int o = 1; o < GRP; o <<= 1) {
+            dot[rr] += __shfl_xor_sync(0xffffffffu, dot[rr], o);
+            na[rr] += __shfl_xor_sync(0xffffffffu, na[rr], o);
+            nb[rr] += __shfl_xor_sync(0xffffffffu, nb[rr], o);
+        }
+        const int gr = r0 + ra + rr;
+        if (t == 0 && gr < rows) {
+            const int hq = kh * g + gr / P.Tq, qi = gr % P.Tq;
+            const float den = sqrtf(na[rr]) * sqrtf(nb[rr]);
+            P.cos_out[(static_cast<int64_t>(l) * P.Hq + hq) * P.Tq + qi] = den > 0.f ? dot[rr] / den : 0.f;
+        }
     }
 }
 

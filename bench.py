@@ -307,6 +307,58 @@ def run_fit(kvb, dev, seed=101, small=False):
     return out
 
 
+def run_fp32_map(kvb, dev, seed=401, reps=3):
+    """The same 14B->32B map at T = 32768 with fp32 caches, maps and output.
+
+    Tensor-core path with every operand carried as a bf16 (hi, lo) pair (three
+    passes); the per-call split of the caches and of W is inside the timing.
+    """
+    import torch
+    import synth
+
+    L_s, L_t, H, d, k, T = W["L_s"], W["L_t"], W["H"], W["d"], W["k"], W["T"]
+    spec = lambda L: {"n_layers": L, "n_kv_heads": H, "head_dim": d, "rope_theta": W["theta_s"]}
+    ctx = kvb.kvb_ctx_create(spec(L_s), spec(L_t), k, T, dev.index or 0)
+    src_k = synth.torch_content(seed, L_s, H, T, d, W["sigma"], torch.float32, dev)
+    src_v = synth.torch_content(seed + 1, L_s, H, T, d, W["sigma"], torch.float32, dev)
+    W_k, b_k = synth.torch_weights(seed + 2, L_t, P_FEAT, Q_OUT, torch.float32, dev)
+    W_v, b_v = synth.torch_weights(seed + 3, L_t, P_FEAT, Q_OUT, torch.float32, dev)
+    sel_k = synth.hidden_selection(seed + 4, L_s, L_t, k)
+    sel_v = synth.hidden_selection(seed + 5, L_s, L_t, k)
+    pos = torch.arange(T, dtype=torch.int32, device=dev)
+    out_k = torch.empty((L_t, H, T, d), dtype=torch.float32, device=dev)
+    out_v = torch.empty_like(out_k)
+    stream = torch.cuda.current_stream(dev)
+    run = lambda: kvb.kvb_map_apply(ctx, src_k, src_v, pos, sel_k, sel_v, W_k, W_v, b_k, b_v, out_k, out_v, stream)
+    run()
+    torch.cuda.synchronize(dev)
+    kvb.kvb_profile_read(ctx)
+    kvb.kvb_profile_enable(ctx, True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    kvb.kvb_profile_enable(ctx, False)
+    kvb.kvb_ctx_check(ctx, stream)
+    ms = e0.elapsed_time(e1) / reps
+    kern = kvb.kvb_profile_read(ctx)
+    g_n, g_ms = kern.get("map_gemm_tcgen05_split3", (0, 0.0))
+    s_n, s_ms = kern.get("split_f32", (0, 0.0))
+    flop = FLOP_PER_TOKEN * T
+    res = {"workload": f"qwen3-14b->32b-shaped map at T={T}, fp32 caches / W / output",
+           "tokens_per_s": T / (ms / 1e3), "ms_per_map": ms,
+           "gemm_kernel": "map_gemm_tcgen05_split3", "gemm_ms": g_ms / max(g_n, 1),
+           "split_ms": s_ms / max(reps, 1),
+           "tflops_algorithmic": flop / (g_ms / max(g_n, 1) / 1e3) / 1e12 if g_ms else None,
+           "tflops_executed_bf16": 3 * flop / (g_ms / max(g_n, 1) / 1e3) / 1e12 if g_ms else None}
+    del src_k, src_v, W_k, W_v, out_k, out_v
+    kvb.kvb_ctx_destroy(ctx)
+    torch.cuda.empty_cache()
+    return res
+
+
 ATTN = dict(L=64, H=8, Hq=64, d=128, n_seq=8, seq_len=256, noise=0.3)
 
 
@@ -548,6 +600,9 @@ def run_gpu(args, rank, world, local_rank):
     attn = None
     if not args.skip_attn:
         attn = run_attention(kvb, dev)
+    fp32_map = None
+    if not args.skip_fp32:
+        fp32_map = run_fp32_map(kvb, dev)
 
     if rank != 0:
         return
@@ -592,6 +647,7 @@ def run_gpu(args, rank, world, local_rank):
                        "double-buffered device buffers"},
         "fit": fit,
         "attention_cosine": attn_roofline(attn, clk),
+        "fp32_map": fp32_map,
         "cpu_baseline": {"value": cpu_rate, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
                          "sample": f"{n_l} of {L_t} target layers x {T_cpu} tokens, float64, scaled to a full map",
                          "seconds": cpu_s},
@@ -611,6 +667,8 @@ def main():
     ap.add_argument("--skip-fit", action="store_true", help="skip the calibration-statistics / fit leg")
     ap.add_argument("--skip-attn", action="store_true", help="skip the attention-output cosine leg")
     ap.add_argument("--attn-only", action="store_true", help="run only the attention-output cosine leg")
+    ap.add_argument("--skip-fp32", action="store_true", help="skip the fp32-cache map leg")
+    ap.add_argument("--fp32-only", action="store_true", help="run only the fp32-cache map leg")
     ap.add_argument("--fit-only", action="store_true", help="run only the fit leg (with --workload small: 8 -> 8 layers)")
     args = ap.parse_args()
     if args.workload == "small":
@@ -623,7 +681,7 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank)
         return
-    if args.fit_only or args.attn_only:
+    if args.fit_only or args.attn_only or args.fp32_only:
         import torch
         from cross_model_kv_gb300 import build as kbuild
         kbuild.build()
@@ -632,6 +690,8 @@ def main():
         torch.cuda.set_device(dev)
         if args.attn_only:
             res = {"attention_cosine": attn_roofline(run_attention(kvb, dev), None)}
+        elif args.fp32_only:
+            res = {"fp32_map": run_fp32_map(kvb, dev)}
         else:
             res = {"fit": run_fit(kvb, dev, small=args.workload == "small")}
         if rank == 0:

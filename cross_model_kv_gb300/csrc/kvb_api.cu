@@ -281,6 +281,61 @@ kvb_status kvb_map_apply(kvb_ctx* c, kvb_dtype dtype, const void* src_k, const v
             if (!why.empty()) return fail(KVB_ERR_CUDA, "map GEMM launch: " + why);
             return cuda_fail(e, "map GEMM launch");
         }
+    } else if (dtype == KVB_F32 && map_gemm_tc_supported(sh)) {
+        // fp32 caches on the tensor cores: stripped keys, values and both
+        // maps are split into bf16 (hi, lo) pairs in the context's scratch,
+        // then one three-pass GEMM accumulates hi*hi + hi*lo + lo*hi in fp32.
+        const size_t n_src = static_cast<size_t>(c->L_s) * c->H * static_cast<size_t>(T) * c->d;
+        const size_t n_w = static_cast<size_t>(c->L_t) * c->H * c->d * static_cast<size_t>(c->k) * c->H * c->d;
+        if ((st = ensure_scratch(c, (4 * n_src + 4 * n_w) * 2)) != KVB_OK) return st;
+        __nv_bfloat16* base = static_cast<__nv_bfloat16*>(c->scratch);
+        __nv_bfloat16* a_hi[2] = {base, base + 2 * n_src};
+        __nv_bfloat16* a_lo[2] = {base + n_src, base + 3 * n_src};
+        __nv_bfloat16* w_hi[2] = {base + 4 * n_src, base + 4 * n_src + 2 * n_w};
+        __nv_bfloat16* w_lo[2] = {base + 4 * n_src + n_w, base + 4 * n_src + 3 * n_w};
+        {
+            ProfScope ps(c, s, "split_f32");
+            e = launch_strip_split_f32(static_cast<const float*>(src_k), a_hi[0], a_lo[0], positions, c->tab_s,
+                                       static_cast<int64_t>(c->L_s) * c->H, T, c->d, c->max_pos, dev_err(c),
+                                       c->num_sms, s);
+            if (e == cudaSuccess)
+                e = launch_split_f32(static_cast<const float*>(src_v), a_hi[1], a_lo[1], static_cast<int64_t>(n_src),
+                                     c->num_sms, s);
+            if (e == cudaSuccess)
+                e = launch_split_f32(static_cast<const float*>(W_k), w_hi[0], w_lo[0], static_cast<int64_t>(n_w),
+                                     c->num_sms, s);
+            if (e == cudaSuccess)
+                e = launch_split_f32(static_cast<const float*>(W_v), w_hi[1], w_lo[1], static_cast<int64_t>(n_w),
+                                     c->num_sms, s);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 split launch");
+        MapGemmArgs a{};
+        a.sh = sh;
+        a.split = true;
+        for (int kv = 0; kv < 2; ++kv) {
+            a.a_src[kv] = a_hi[kv];
+            a.a_lo[kv] = a_lo[kv];
+            a.w[kv] = w_hi[kv];
+            a.w_lo[kv] = w_lo[kv];
+        }
+        a.bias[0] = b_k;
+        a.bias[1] = b_v;
+        a.out[0] = out_k;
+        a.out[1] = out_v;
+        a.pos = positions;
+        a.tab_t = c->tab_t;
+        a.sel = tab;
+        a.err = dev_err(c);
+        a.num_sms = c->num_sms;
+        std::string why;
+        {
+            ProfScope ps(c, s, "map_gemm_tcgen05_split3");
+            e = launch_map_gemm_tc(a, s, &why);
+        }
+        if (e != cudaSuccess) {
+            if (!why.empty()) return fail(KVB_ERR_CUDA, "map GEMM launch: " + why);
+            return cuda_fail(e, "map GEMM launch");
+        }
     } else {
         MapSimtArgs a{};
         a.sh = sh;

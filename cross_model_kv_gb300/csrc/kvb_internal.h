@@ -37,13 +37,27 @@ cudaError_t launch_strip_bf16(const __nv_bfloat16* in, __nv_bfloat16* out, const
                               const float2* tab, int64_t LH, int64_t T, int d, int max_pos,
                               DevErr err, int num_sms, cudaStream_t s);
 
-// tcgen05 mapper GEMM with fused bias + target RoPE epilogue (bf16, d == 128).
+// fp32 operands as bf16 (hi, lo) pairs for the tensor-core map: strip fp32
+// keys [LH][T][d] and split them; split n fp32 values (n % 8 == 0).
+cudaError_t launch_strip_split_f32(const float* in, __nv_bfloat16* hi, __nv_bfloat16* lo, const int* pos,
+                                   const float2* tab, int64_t LH, int64_t T, int d, int max_pos, DevErr err,
+                                   int num_sms, cudaStream_t s);
+cudaError_t launch_split_f32(const float* in, __nv_bfloat16* hi, __nv_bfloat16* lo, int64_t n, int num_sms,
+                             cudaStream_t s);
+
+// tcgen05 mapper GEMM with fused bias + target RoPE epilogue (d == 128).  With
+// split set, operands are fp32 values carried as bf16 (hi, lo) pairs: the
+// accumulation runs hi*hi + hi*lo + lo*hi and the output is fp32; otherwise
+// bf16 operands and bf16 output.
 struct MapGemmArgs {
     Shape sh;
-    const void* a_src[2];   // [L_s*H][T][d] bf16: stripped keys, raw values
-    const void* w[2];       // [L_t][q][p] bf16
+    const void* a_src[2];   // [L_s*H][T][d] bf16: stripped keys, raw values (hi parts when split)
+    const void* w[2];       // [L_t][q][p] bf16 (hi parts when split)
+    const void* a_lo[2];    // lo parts when split
+    const void* w_lo[2];
+    bool split;
     const float* bias[2];   // [L_t][q]
-    void* out[2];           // [L_t][H][T][d] bf16
+    void* out[2];           // [L_t][H][T][d] bf16 (fp32 when split)
     const int* pos;
     const float2* tab_t;    // target RoPE table
     SelTable sel;

@@ -22,6 +22,8 @@
 // registers, + bias, target RoPE for K (pairs (e, e+64) of one head are in the
 // same tile), round to bf16, store straight into the target cache
 // [t][h][token][e].  Accumulators are double buffered in TMEM (2 x 256 columns).
+// fp32 caches run through the single-CTA kernel with each operand carried as
+// a bf16 (hi, lo) pair and an fp32 output (map_gemm_kernel<true>).
 // Every wait is bounded (DevErr::timeout_ns); on expiry the CTA records
 // DEV_ERR_TIMEOUT, stops, drains its copies and MMAs and frees TMEM.
 #include <cstdlib>
@@ -65,7 +67,7 @@ struct Params {
     int L_t, H, d, T, num_m, num_n, nk, total_tiles, max_pos;
     const int* pos;
     const float* bias[2];
-    __nv_bfloat16* out[2];
+    void* out[2];          // bf16, or fp32 for the split (fp32-operand) kernel
     const float2* tab_t;
     DevErr err;
     SelTable sel;
@@ -98,7 +100,8 @@ __device__ __forceinline__ void kblock_source(const Params& P, int kv, int t, in
 }
 
 // One thread's row of one accumulator tile (256 columns = two heads): bias,
-// target RoPE for keys, bf16 rounding, store into [t][h][tok][e].
+// target RoPE for keys, bf16 rounding (or fp32 as is), store into [t][h][tok][e].
+template <bool F32OUT>
 __device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c, int tok, uint32_t tbase, int q) {
     const bool valid = tok < P.T;
     int p = valid ? __ldg(P.pos + tok) : 0;
@@ -114,7 +117,7 @@ __device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c
     const float2* tab = P.tab_t + static_cast<int64_t>(p) * half;
     for (int hh = 0; hh < heads_per_tile; ++hh) {
         const int h = c.n * heads_per_tile + hh;
-        __nv_bfloat16* orow = P.out[c.kv] + ((static_cast<int64_t>(c.t) * P.H + h) * P.T + tok) * P.d;
+        const int64_t orow = ((static_cast<int64_t>(c.t) * P.H + h) * P.T + tok) * P.d;
 #pragma unroll 1
         for (int e0 = 0; e0 < half; e0 += 16) {
             uint32_t lo[16], hi[16];
@@ -150,27 +153,46 @@ __device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c
                     xh[2 * v + 1] = fmaf(h1, cs.z, l1 * cs.w);
                 }
             }
-            if (valid) {
+            if (valid && F32OUT) {
+                float* o = static_cast<float*>(P.out[c.kv]) + orow;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const float4 a = bad_pos ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                             : make_float4(xl[4 * v], xl[4 * v + 1], xl[4 * v + 2], xl[4 * v + 3]);
+                    const float4 b = bad_pos ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                             : make_float4(xh[4 * v], xh[4 * v + 1], xh[4 * v + 2], xh[4 * v + 3]);
+                    *reinterpret_cast<float4*>(o + e0 + 4 * v) = a;
+                    *reinterpret_cast<float4*>(o + half + e0 + 4 * v) = b;
+                }
+            } else if (valid) {
+                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(P.out[c.kv]) + orow;
                 uint32_t pl[8], ph[8];
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
                     pl[v] = bad_pos ? 0u : pack_bf16x2(xl[2 * v], xl[2 * v + 1]);
                     ph[v] = bad_pos ? 0u : pack_bf16x2(xh[2 * v], xh[2 * v + 1]);
                 }
-                st_global_v4(orow + e0, make_uint4(pl[0], pl[1], pl[2], pl[3]));
-                st_global_v4(orow + e0 + 8, make_uint4(pl[4], pl[5], pl[6], pl[7]));
-                st_global_v4(orow + half + e0, make_uint4(ph[0], ph[1], ph[2], ph[3]));
-                st_global_v4(orow + half + e0 + 8, make_uint4(ph[4], ph[5], ph[6], ph[7]));
+                st_global_v4(o + e0, make_uint4(pl[0], pl[1], pl[2], pl[3]));
+                st_global_v4(o + e0 + 8, make_uint4(pl[4], pl[5], pl[6], pl[7]));
+                st_global_v4(o + half + e0, make_uint4(ph[0], ph[1], ph[2], ph[3]));
+                st_global_v4(o + half + e0 + 8, make_uint4(ph[4], ph[5], ph[6], ph[7]));
             }
         }
     }
 }
 
 // ============================================================ single CTA
+// SPLIT: the operands are fp32 values carried as bf16 (hi, lo) pairs; each
+// 64-wide K block is issued three times (A hi x W hi, A hi x W lo, A lo x W
+// hi) into the same accumulator and the output is fp32.
+template <bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     map_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                     const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+                    const __grid_constant__ CUtensorMap tm_a0l, const __grid_constant__ CUtensorMap tm_a1l,
+                    const __grid_constant__ CUtensorMap tm_w0l, const __grid_constant__ CUtensorMap tm_w1l,
                     const __grid_constant__ Params P) {
+    constexpr int NSEG = SPLIT ? 3 : 1;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -205,6 +227,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tm_a1);
         tma_prefetch_desc(&tm_w0);
         tma_prefetch_desc(&tm_w1);
+        if (SPLIT) {
+            tma_prefetch_desc(&tm_a0l);
+            tma_prefetch_desc(&tm_a1l);
+            tma_prefetch_desc(&tm_w0l);
+            tma_prefetch_desc(&tm_w1l);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -216,6 +244,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     const int q = P.H * P.d;
+    const int nk_issue = P.nk * NSEG;  // K blocks issued per tile
 
     if (warp == 0) {
         if (lane == 0) {
@@ -227,9 +256,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
                 const TileCoord c = decode_tile(P, tile);
-                const CUtensorMap* ta = c.kv ? &tm_a1 : &tm_a0;
-                const CUtensorMap* tw = c.kv ? &tm_w1 : &tm_w0;
-                for (int kb = 0; kb < P.nk; ++kb) {
+                for (int ki = 0; ki < nk_issue; ++ki) {
+                    const int kb = SPLIT ? ki / 3 : ki;
+                    const int seg = SPLIT ? ki - 3 * kb : 0;  // 0: hi x hi, 1: hi x lo, 2: lo x hi
+                    const CUtensorMap* ta = seg == 2 ? (c.kv ? &tm_a1l : &tm_a0l) : (c.kv ? &tm_a1 : &tm_a0);
+                    const CUtensorMap* tw = seg == 1 ? (c.kv ? &tm_w1l : &tm_w0l) : (c.kv ? &tm_w1 : &tm_w0);
                     if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) {
                         ok = false;
                         break;
@@ -263,7 +294,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, P.err, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < P.nk; ++kb) {
+                for (int kb = 0; kb < nk_issue; ++kb) {
                     if (!mbar_wait(&full[stage], phase, P.err, abort_flag)) {
                         ok = false;
                         break;
@@ -302,7 +333,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!mbar_wait(&tfull[acc], acc_phase, P.err, abort_flag)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            epilogue_row(P, c, c.m * BM + row, tbase, q);
+            epilogue_row<SPLIT>(P, c, c.m * BM + row, tbase, q);
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
             acc ^= 1;
@@ -468,7 +499,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!mbar_wait(&tfull[acc], acc_phase, P.err, abort_flag)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            epilogue_row(P, c, c.m * PM + 128 * static_cast<int>(rank) + row, tbase, q);
+            epilogue_row<false>(P, c, c.m * PM + 128 * static_cast<int>(rank) + row, tbase, q);
             tc_fence_before();
             mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
             acc ^= 1;
@@ -522,7 +553,7 @@ cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string
     const Shape& sh = a.sh;
     const int q = sh.H * sh.d;
     const int p = sh.k * q;
-    const bool pair = use_pair_kernel() && a.num_sms >= 2;
+    const bool pair = !a.split && use_pair_kernel() && a.num_sms >= 2;
     const int tm = pair ? PM : BM;
     Params P{};
     P.L_t = sh.L_t;
@@ -545,19 +576,30 @@ cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string
     P.sel = a.sel;
     for (int kv = 0; kv < 2; ++kv) {
         P.bias[kv] = a.bias[kv];
-        P.out[kv] = static_cast<__nv_bfloat16*>(a.out[kv]);
+        P.out[kv] = a.out[kv];
     }
-    CUtensorMap tma[2], tmw[2];
+    CUtensorMap tma[2], tmw[2], tmal[2], tmwl[2];
     for (int kv = 0; kv < 2; ++kv) {
         if (!encode_3d_bf16(&tma[kv], a.a_src[kv], sh.d, sh.T, static_cast<uint64_t>(sh.L_s) * sh.H, BK, 128, why))
             return cudaErrorInvalidValue;
         if (!encode_3d_bf16(&tmw[kv], a.w[kv], p, q, sh.L_t, BK, pair ? 128 : BN, why)) return cudaErrorInvalidValue;
+        if (a.split) {
+            if (!encode_3d_bf16(&tmal[kv], a.a_lo[kv], sh.d, sh.T, static_cast<uint64_t>(sh.L_s) * sh.H, BK, 128,
+                                why))
+                return cudaErrorInvalidValue;
+            if (!encode_3d_bf16(&tmwl[kv], a.w_lo[kv], p, q, sh.L_t, BK, BN, why)) return cudaErrorInvalidValue;
+        } else {
+            tmal[kv] = tma[kv];  // unused by the bf16 kernel
+            tmwl[kv] = tmw[kv];
+        }
     }
     if (!pair) {
-        cudaError_t e = cudaFuncSetAttribute(map_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        auto kern = a.split ? map_gemm_kernel<true> : map_gemm_kernel<false>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         const int grid = static_cast<int>(total < a.num_sms ? total : a.num_sms);
-        map_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tma[0], tma[1], tmw[0], tmw[1], P);
+        kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tma[0], tma[1], tmw[0], tmw[1], tmal[0], tmal[1], tmwl[0], tmwl[1],
+                                                   P);
         return cudaGetLastError();
     }
     cudaError_t e = cudaFuncSetAttribute(map_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PSMEM_BYTES);

@@ -127,7 +127,14 @@ kvb_status kvb_profile_read(kvb_ctx* ctx, kvb_kernel_time* out, int32_t cap, int
  * Map a source cache into a target cache ("Cross-Model KV Transfer", "The
  * mapping"; "KV-Cache zwischen Qwen3-Modellen ...", map_cache sketch).
  *   dtype       KVB_BF16: bf16 caches and W, fp32 accumulation, bf16 output
- *                         (round to nearest even); KVB_F32: fp32 throughout.
+ *                         (round to nearest even); KVB_F32: fp32 caches, W and
+ *                         output.  With head_dim 128 and H*d a multiple of 256
+ *                         both run on the tensor cores; KVB_F32 then carries
+ *                         every operand as a bf16 (hi, lo) pair, accumulates
+ *                         hi*hi + hi*lo + lo*hi in fp32 (relative error near
+ *                         2^-16 per product) and splits W on every call into
+ *                         context scratch (4*(L_src*H*T*d + L_tgt*q*p) * 2
+ *                         bytes in all); other shapes run fp32 on CUDA cores.
  *   src_k/src_v device [L_src][H][T][d] (keys as stored, i.e. with source RoPE)
  *   positions   device [T] int32
  *   sel_k/sel_v host   [L_tgt][k] int32, entries distinct within a row, in range

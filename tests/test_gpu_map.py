@@ -32,8 +32,9 @@ def _check_all(kvb, c, max_pos, tol, layers=None, tokens=None):
     c.run(kvb, ctx)
     kvb.kvb_ctx_check(ctx)
     ran = kvb.kvb_profile_read(ctx)
-    tensor_core = c.dtype == torch.bfloat16 and c.d == 128 and (c.H * c.d) % 256 == 0
-    assert ("map_gemm_tcgen05" in ran) == tensor_core and ("map_simt" in ran) != tensor_core, ran
+    tensor_core = c.d == 128 and (c.H * c.d) % 256 == 0
+    tc_name = "map_gemm_tcgen05" if c.dtype == torch.bfloat16 else "map_gemm_tcgen05_split3"
+    assert (tc_name in ran) == tensor_core and ("map_simt" in ran) != tensor_core, ran
     ok, ov = c.oracle(layers, tokens)
     gk, gv = c.gpu(layers, tokens)
     ek, ev = rel_fro(gk, ok), rel_fro(gv, ov)
@@ -78,9 +79,39 @@ def test_bf16_cuda_core_path_head_dim_64(kvb):
     _check_all(kvb, c, 256, TOL_BF16)
 
 
-def test_fp32_head_dim_128(kvb):
+def test_fp32_tensor_core_split_head_dim_128(kvb):
+    # fp32 caches on the tensor cores (bf16 hi/lo operand pairs, three passes)
     c = ApplyCase(3, 2, 2, 128, 2, 130, 1e6, 5e5, torch.float32, seed=25, positions=np.arange(130) * 200)
     _check_all(kvb, c, 32768, TOL_F32)
+
+
+def test_fp32_tensor_core_split_ragged_tail_two_n_tiles(kvb):
+    # 4 KV heads (two 256-wide output tiles), T = 1001 (ragged last token block), random positions
+    pos = np.random.default_rng(5).integers(0, 30000, size=1001).astype(np.int32)
+    c = ApplyCase(5, 3, 4, 128, 3, 1001, 1e4, 1e6, torch.float32, seed=34, positions=pos)
+    ek, ev = _check_all(kvb, c, 30000, TOL_F32)
+    assert ek < 2e-5 and ev < 2e-5, (ek, ev)  # the split keeps ~16 bits per operand
+
+
+def test_fp32_cuda_core_path_head_dim_128_one_head(kvb):
+    # one KV head (H*d = 128, not a multiple of the 256-wide output tile): CUDA cores
+    c = ApplyCase(3, 2, 1, 128, 2, 70, 1e6, 5e5, torch.float32, seed=35, positions=np.arange(70) * 100)
+    _check_all(kvb, c, 8192, TOL_F32)
+
+
+def test_fp32_bad_position_is_reported_and_row_zeroed(kvb):
+    pos = np.arange(200, dtype=np.int32)
+    pos[33] = -4
+    c = ApplyCase(2, 2, 2, 128, 1, 200, 1e4, 1e6, torch.float32, seed=36, positions=pos)
+    ctx = _ctx(kvb, c, 256)
+    c.run(kvb, ctx)
+    with pytest.raises(kvb.KvbError) as e:
+        kvb.kvb_ctx_check(ctx)
+    assert e.value.status == 1
+    assert torch.count_nonzero(c.out_k[:, :, 33]).item() == 0
+    assert torch.count_nonzero(c.out_v[:, :, 33]).item() == 0
+    assert torch.count_nonzero(c.out_k[:, :, 32]).item() > 0
+    kvb.kvb_ctx_check(ctx)
 
 
 def test_empty_input_is_a_no_op(kvb):
@@ -146,6 +177,14 @@ def test_qwen3_14b_to_32b_shape_T32768(kvb):
     # 40 -> 64 layers, 8 KV heads, head_dim 128, theta 1e6, k = 8, T = 32768
     c = ApplyCase(40, 64, 8, 128, 8, 32768, 1e6, 1e6, torch.bfloat16, seed=32, host=False)
     _check_all(kvb, c, 32768, TOL_BF16, layers=[0, 31, 63], tokens=_sampled_tokens(32768, 384, 2))
+    del c
+    torch.cuda.empty_cache()
+
+
+def test_qwen3_14b_to_32b_shape_fp32_T4096(kvb):
+    # fp32 caches and maps at the 14B -> 32B shape on the split tensor-core path
+    c = ApplyCase(40, 64, 8, 128, 8, 4096, 1e6, 1e6, torch.float32, seed=37, host=False)
+    _check_all(kvb, c, 4096, TOL_F32, layers=[0, 40, 63], tokens=_sampled_tokens(4096, 256, 4))
     del c
     torch.cuda.empty_cache()
 

@@ -223,8 +223,10 @@ __device__ __forceinline__ void pair8(const __nv_bfloat16* __restrict__ row, int
 
 constexpr int kChunk = 128;  // kept rows per CTA of the single-pass gather
 
-// Grid (slab, 128-row chunk), 256 threads; each thread owns R rows of its lane
-// column (R = 128 / rows-per-sweep) and issues all their loads before any use.
+// Grid (chunk group, slab), 256 threads; a CTA takes chunks blockIdx.x,
+// blockIdx.x + gridDim.x, ... of its slab (the host sizes gridDim.x from
+// T / stride, so few CTAs find no kept rows).  Each thread owns R rows of its
+// lane column (R = 128 / rows-per-sweep) and issues all their loads before any use.
 // Writes z = feature - s transposed ([f][r], float32 or bf16 hi/lo), the
 // chunk's column sums of z to part[chunk][slab*d + e], and (chunk 0) the shift.
 template <int R>
@@ -238,13 +240,11 @@ __global__ void __launch_bounds__(256, (R <= 4 ? 2 : 1)) gather_shift_kernel(con
                                                            float* __restrict__ shift_out, float* __restrict__ part,
                                                            int64_t F, void* __restrict__ out,
                                                            void* __restrict__ out_lo, int64_t ld) {
-    extern __shared__ float tile[];  // [d][kChunk + 1] then [rps][d] partial sums
+    extern __shared__ float tile[];  // [d][kChunk + 1] then [8 warps][d] partial sums
     constexpr int LT = kChunk + 1;
     const int slab = blockIdx.y;  // chunks of one slab run side by side: contiguous reads and writes
-    const int chunk = blockIdx.x;
-    const int r0 = chunk * kChunk;
     const int n = *nb;
-    if (r0 >= ((n + kChunk - 1) / kChunk) * kChunk) return;
+    if (static_cast<int>(blockIdx.x) * kChunk >= n) return;
     const int half = d >> 1;
     const int lpr = d >> 4;          // lanes per row (8 pairs each)
     const int rps = 256 / lpr;       // rows per sweep
@@ -253,6 +253,29 @@ __global__ void __launch_bounds__(256, (R <= 4 ? 2 : 1)) gather_shift_kernel(con
     const __nv_bfloat16* base = cache + static_cast<int64_t>(slab) * T_len * d;
     const int64_t f0 = static_cast<int64_t>(slab) * d;
 
+    float slo[8], shi[8];
+    if (*n_seen > 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            slo[i] = mean_a[f0 + 8 * l + i];
+            shi[i] = mean_a[f0 + half + 8 * l + i];
+        }
+    } else {  // first batch: shift by the first kept row (n >= 1 here)
+        const int tok = __ldg(rows);
+        pair8(base + static_cast<int64_t>(tok) * d, l, half, strip, tab + static_cast<int64_t>(__ldg(pos + tok)) * half,
+              slo, shi);
+    }
+    if (blockIdx.x == 0 && rq == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            shift_out[f0 + 8 * l + i] = slo[i];
+            shift_out[f0 + half + 8 * l + i] = shi[i];
+        }
+    }
+
+#pragma unroll 1
+    for (int chunk = blockIdx.x; chunk * kChunk < n; chunk += gridDim.x) {
+    const int r0 = chunk * kChunk;
     // issue every load of this thread's rows first
     uint4 ra[R], rb[R];
     float4 cs[R][4];
@@ -274,25 +297,6 @@ __global__ void __launch_bounds__(256, (R <= 4 ? 2 : 1)) gather_shift_kernel(con
         }
     }
 
-    float slo[8], shi[8];
-    if (*n_seen > 0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            slo[i] = mean_a[f0 + 8 * l + i];
-            shi[i] = mean_a[f0 + half + 8 * l + i];
-        }
-    } else {  // first batch: shift by the first kept row (n >= 1 here)
-        const int tok = __ldg(rows);
-        pair8(base + static_cast<int64_t>(tok) * d, l, half, strip, tab + static_cast<int64_t>(__ldg(pos + tok)) * half,
-              slo, shi);
-    }
-    if (chunk == 0 && rq == 0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            shift_out[f0 + 8 * l + i] = slo[i];
-            shift_out[f0 + half + 8 * l + i] = shi[i];
-        }
-    }
     float alo[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, ahi[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < R; ++u) {
@@ -326,16 +330,27 @@ __global__ void __launch_bounds__(256, (R <= 4 ? 2 : 1)) gather_shift_kernel(con
             tile[(half + 8 * l + i) * LT + rr] = zh[i];
         }
     }
+    // column sums: across the warp's rows by shuffles, then across the 8 warps
     float* red = tile + d * LT;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        red[rq * d + 8 * l + i] = alo[i];
-        red[rq * d + half + 8 * l + i] = ahi[i];
+        for (int o = lpr; o < 32; o <<= 1) {
+            alo[i] += __shfl_xor_sync(0xffffffffu, alo[i], o);
+            ahi[i] += __shfl_xor_sync(0xffffffffu, ahi[i], o);
+        }
+    }
+    const int wq = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) < lpr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            red[wq * d + 8 * l + i] = alo[i];
+            red[wq * d + half + 8 * l + i] = ahi[i];
+        }
     }
     __syncthreads();
     for (int e = threadIdx.x; e < d; e += blockDim.x) {
         float s = 0.f;
-        for (int q = 0; q < rps; ++q) s += red[q * d + e];
+        for (int q = 0; q < 8; ++q) s += red[q * d + e];
         part[static_cast<int64_t>(chunk) * F + f0 + e] = s;
     }
     if (out_lo == nullptr) {
@@ -362,6 +377,204 @@ __global__ void __launch_bounds__(256, (R <= 4 ? 2 : 1)) gather_shift_kernel(con
             *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + o) = make_uint4(h[0], h[1], h[2], h[3]);
             *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_lo) + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
+    }
+    __syncthreads();  // the tile and the sums are reused by the next chunk
+    }
+}
+
+// Streaming variant of the single-pass gather (head_dim 64 or 128).  A CTA
+// owns one 128-row chunk at a time and walks slabs blockIdx.y, blockIdx.y +
+// gridDim.y, ... of it.  Per chunk the kept-row indices, positions and (for
+// keys) the chunk's RoPE table rows are staged in shared memory once; per
+// slab the raw rows are copied in with cp.async, kStages - 1 slabs ahead of
+// the one being processed.  Thread (pair i, row group q) strips pair
+// (i, i + d/2) of rows 16q .. 16q + 15 straight from shared memory, keeps its
+// centered values in registers, writes them as bf16 (hi, lo) runs of its
+// observations into the feature-major outputs and sums them per column: no
+// transpose through shared memory.
+constexpr int kStages = 3;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// One 32-byte global store (sm_100 and later); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// Threads of the streaming gather: every thread keeps 16 rows of one RoPE pair.
+__host__ __device__ constexpr int stream_threads(int d) { return kChunk * (d / 2) / 16; }
+
+size_t gather_stream_smem(int d) {
+    return static_cast<size_t>(kStages) * kChunk * d * 2   // raw rows
+           + static_cast<size_t>(kStages) * d * 4          // running means of the staged slabs
+           + static_cast<size_t>(kChunk) * (d / 2) * 8     // RoPE table rows of the chunk
+           + static_cast<size_t>(stream_threads(d) / (d / 2)) * d * 4  // per-row-group column sums
+           + 2 * kChunk * 4;                               // row indices, positions
+}
+
+template <int D>
+__global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(const __nv_bfloat16* __restrict__ cache, int64_t T_len,
+                                                               const int* __restrict__ rows,
+                                                               const int* __restrict__ nb,
+                                                               const long long* __restrict__ n_seen,
+                                                               const int* __restrict__ pos,
+                                                               const float2* __restrict__ tab, bool strip,
+                                                               const float* __restrict__ mean_a,
+                                                               float* __restrict__ shift_out, float* __restrict__ part,
+                                                               int64_t F, __nv_bfloat16* __restrict__ out,
+                                                               __nv_bfloat16* __restrict__ out_lo, int64_t ld,
+                                                               int n_slabs) {
+    constexpr int HALF = D / 2;
+    constexpr int QN = stream_threads(D) / HALF;  // row groups
+    constexpr int ROWS = kChunk / QN;             // rows per thread (16)
+    static_assert(ROWS % 16 == 0, "whole 32-byte output runs per thread");
+    constexpr int PIECES = kChunk * (D / 8);
+    extern __shared__ __align__(16) uint8_t gsm[];
+    __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(gsm);
+    float* smean = reinterpret_cast<float*>(gsm + static_cast<size_t>(kStages) * kChunk * D * 2);
+    float2* stab = reinterpret_cast<float2*>(smean + kStages * D);
+    float* red = reinterpret_cast<float*>(stab + kChunk * HALF);
+    int* srow = reinterpret_cast<int*>(red + QN * D);
+    int* spos = srow + kChunk;
+    const int n = *nb;
+    const int i = threadIdx.x % HALF;  // RoPE pair (i, i + D/2)
+    const int q = threadIdx.x / HALF;  // rows q*ROWS .. q*ROWS + ROWS - 1 of the chunk
+    const bool first_batch = *n_seen == 0;
+
+#pragma unroll 1
+    for (int chunk = blockIdx.x; chunk * kChunk < n; chunk += gridDim.x) {
+        const int r0 = chunk * kChunk;
+        __syncthreads();  // the previous chunk is done with srow / spos / stab
+        for (int t = threadIdx.x; t < kChunk; t += blockDim.x) {
+            const int r = r0 + t;
+            const int tok = r < n ? __ldg(rows + r) : -1;
+            srow[t] = tok;
+            spos[t] = tok >= 0 ? __ldg(pos + tok) : 0;
+        }
+        __syncthreads();
+        if (strip) {  // the chunk's table rows ride in the first copy group
+            for (int pc = threadIdx.x; pc < kChunk * (HALF / 2); pc += blockDim.x) {
+                const int rr = pc / (HALF / 2), c2 = (pc % (HALF / 2)) * 2;
+                cp_async16(stab + rr * HALF + c2, tab + static_cast<int64_t>(spos[rr]) * HALF + c2, 16);
+            }
+        }
+        const int mine = (n_slabs - static_cast<int>(blockIdx.y) + static_cast<int>(gridDim.y) - 1) /
+                         static_cast<int>(gridDim.y);
+        auto issue = [&](int j) {  // raw rows (and running means) of this CTA's j-th slab into stage j % kStages
+            const int slab = blockIdx.y + j * gridDim.y;
+            const __nv_bfloat16* base = cache + static_cast<int64_t>(slab) * T_len * D;
+            __nv_bfloat16* dst = stg + static_cast<size_t>(j % kStages) * kChunk * D;
+            if (!first_batch && threadIdx.x < D / 4)
+                cp_async16(smean + (j % kStages) * D + 4 * threadIdx.x, mean_a + static_cast<int64_t>(slab) * D +
+                           4 * threadIdx.x, 16);
+            for (int pc = threadIdx.x; pc < PIECES; pc += blockDim.x) {
+                const int rr = pc / (D / 8), c8 = (pc % (D / 8)) * 8;
+                const int tok = srow[rr];
+                cp_async16(dst + rr * D + c8, tok >= 0 ? base + static_cast<int64_t>(tok) * D + c8 : cache,
+                           tok >= 0 ? 16 : 0);
+            }
+        };
+#pragma unroll
+        for (int j = 0; j < kStages - 1; ++j) {
+            if (j < mine) issue(j);
+            cp_async_commit();
+        }
+#pragma unroll 1
+        for (int j = 0; j < mine; ++j) {
+            if (j + kStages - 1 < mine) issue(j + kStages - 1);
+            cp_async_commit();
+            cp_async_wait<kStages - 1>();
+            __syncthreads();  // every thread's copies of slab j (and the table) have landed
+
+            const int slab = blockIdx.y + j * gridDim.y;
+            const int64_t f0 = static_cast<int64_t>(slab) * D;
+            const __nv_bfloat16* raw = stg + static_cast<size_t>(j % kStages) * kChunk * D;
+            float sl, sh;  // shift of features i and i + D/2
+            if (!first_batch) {
+                sl = smean[(j % kStages) * D + i];
+                sh = smean[(j % kStages) * D + HALF + i];
+            } else {  // first batch: shift by the first kept row (n >= 1 here)
+                const int tok = __ldg(rows);
+                const __nv_bfloat16* row0 = cache + static_cast<int64_t>(slab) * T_len * D + static_cast<int64_t>(tok) * D;
+                const float x = __bfloat162float(row0[i]), y = __bfloat162float(row0[HALF + i]);
+                if (strip) {
+                    const float2 cs = __ldg(tab + static_cast<int64_t>(__ldg(pos + tok)) * HALF + i);
+                    sl = fmaf(x, cs.x, y * cs.y);
+                    sh = fmaf(y, cs.x, -(x * cs.y));
+                } else {
+                    sl = x;
+                    sh = y;
+                }
+            }
+            if (chunk == 0 && q == 0) {
+                shift_out[f0 + i] = sl;
+                shift_out[f0 + HALF + i] = sh;
+            }
+            float zl[ROWS], zh[ROWS];
+            float al = 0.f, ah = 0.f;
+#pragma unroll
+            for (int u = 0; u < ROWS; ++u) {
+                const int rr = q * ROWS + u;
+                const float x = __bfloat162float(raw[rr * D + i]);
+                const float y = __bfloat162float(raw[rr * D + HALF + i]);
+                float a = x, b = y;
+                if (strip) {
+                    const float2 cs = stab[rr * HALF + i];
+                    a = fmaf(x, cs.x, y * cs.y);
+                    b = fmaf(y, cs.x, -(x * cs.y));
+                }
+                const bool valid = srow[rr] >= 0;
+                zl[u] = valid ? a - sl : 0.f;
+                zh[u] = valid ? b - sh : 0.f;
+                al += zl[u];
+                ah += zh[u];
+            }
+            // feature-major outputs: ROWS consecutive observations per feature
+            const int64_t ol = (f0 + i) * ld + r0 + q * ROWS;
+            const int64_t oh = (f0 + HALF + i) * ld + r0 + q * ROWS;
+            // 16 observations (32 bytes, one sector) per store
+#pragma unroll
+            for (int v = 0; v < ROWS / 16; ++v) {
+                uint32_t hl[8], ll[8], hh[8], lh[8];
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const int u = 16 * v + 2 * w;
+                    const __nv_bfloat162 b0 = __floats2bfloat162_rn(zl[u], zl[u + 1]);
+                    const float2 f0v = __bfloat1622float2(b0);
+                    hl[w] = *reinterpret_cast<const uint32_t*>(&b0);
+                    ll[w] = pack_bf16x2(zl[u] - f0v.x, zl[u + 1] - f0v.y);
+                    const __nv_bfloat162 b1 = __floats2bfloat162_rn(zh[u], zh[u + 1]);
+                    const float2 f1v = __bfloat1622float2(b1);
+                    hh[w] = *reinterpret_cast<const uint32_t*>(&b1);
+                    lh[w] = pack_bf16x2(zh[u] - f1v.x, zh[u + 1] - f1v.y);
+                }
+                st_global_v8(out + ol + 16 * v, hl);
+                st_global_v8(out_lo + ol + 16 * v, ll);
+                st_global_v8(out + oh + 16 * v, hh);
+                st_global_v8(out_lo + oh + 16 * v, lh);
+            }
+            red[q * D + i] = al;
+            red[q * D + HALF + i] = ah;
+            __syncthreads();
+            for (int e = threadIdx.x; e < D; e += blockDim.x) {
+                float sm = 0.f;
+#pragma unroll
+                for (int g = 0; g < QN; ++g) sm += red[g * D + e];
+                part[static_cast<int64_t>(chunk) * F + f0 + e] = sm;
+            }
+            __syncthreads();  // stage j % kStages and the sums are free again
+        }
+        cp_async_wait<0>();
     }
 }
 
@@ -524,8 +737,40 @@ cudaError_t launch_gather(const GatherArgs& g, cudaStream_t s) {
     if (gather_single_pass_ok(g.dt, g.d)) {
         const int rps = 256 / (g.d >> 4);
         const int R = rps >= kChunk ? 1 : kChunk / rps;
-        const size_t smem = (static_cast<size_t>(g.d) * (kChunk + 1) + static_cast<size_t>(rps) * g.d) * sizeof(float);
-        dim3 cgrid(static_cast<unsigned>((g.T + kChunk - 1) / kChunk), static_cast<unsigned>(g.n_slabs));
+        if (g.out_lo != nullptr && (g.d == 64 || g.d == 128) && g.num_sms > 0) {
+            const int64_t n_guess = (g.T + g.stride - 1) / g.stride;
+            int64_t gx = (n_guess + kChunk - 1) / kChunk;
+            if (gx > g.num_sms) gx = g.num_sms;
+            if (gx < 1) gx = 1;
+            int64_t gy = g.num_sms / gx;
+            if (gy > g.n_slabs) gy = g.n_slabs;
+            if (gy < 1) gy = 1;
+            dim3 sgrid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+            const size_t smem = gather_stream_smem(g.d);
+            const __nv_bfloat16* c16 = static_cast<const __nv_bfloat16*>(g.cache);
+            __nv_bfloat16* o16 = static_cast<__nv_bfloat16*>(g.out);
+            __nv_bfloat16* l16 = static_cast<__nv_bfloat16*>(g.out_lo);
+#define KVB_STREAM(DD)                                                                                             \
+    do {                                                                                                           \
+        cudaError_t e = cudaFuncSetAttribute(gather_stream_kernel<DD>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                             static_cast<int>(smem));                                              \
+        if (e != cudaSuccess) return e;                                                                            \
+        gather_stream_kernel<DD><<<sgrid, stream_threads(DD), smem, s>>>(c16, g.T, g.rows, g.nb, g.n_seen, g.pos, g.tab, g.strip, \
+                                                          g.mean_a, g.shift, g.part, F, o16, l16, g.ld,            \
+                                                          static_cast<int>(g.n_slabs));                            \
+    } while (0)
+            switch (g.d) {
+                case 64: KVB_STREAM(64); break;
+                default: KVB_STREAM(128); break;
+            }
+#undef KVB_STREAM
+            zsum_kernel<<<static_cast<unsigned>((F + 255) / 256), 256, 0, s>>>(g.part, F, g.nb, g.zsum);
+            return cudaGetLastError();
+        }
+        const size_t smem = (static_cast<size_t>(g.d) * (kChunk + 1) + 8 * static_cast<size_t>(g.d)) * sizeof(float);
+        // kept rows are about T / stride; a CTA loops if there are more
+        const int64_t n_guess = (g.T + g.stride - 1) / g.stride;
+        dim3 cgrid(static_cast<unsigned>((n_guess + kChunk - 1) / kChunk), static_cast<unsigned>(g.n_slabs));
         const __nv_bfloat16* c16 = static_cast<const __nv_bfloat16*>(g.cache);
 #define KVB_GATHER(RR)                                                                                          \
     do {                                                                                                        \

@@ -287,6 +287,8 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
             g.cache = caches[m];
             g.n_slabs = slabs[m];
             g.T = T;
+            g.stride = stride > 1 ? stride : 1;
+            g.num_sms = c->num_sms;
             g.d = c->d;
             g.rows = st->rows;
             g.nb = st->nb_dev;

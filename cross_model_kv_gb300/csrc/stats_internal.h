@@ -23,6 +23,8 @@ struct GatherArgs {
     kvb_dtype dt;
     const void* cache;
     int64_t n_slabs, T;
+    int stride;               // positions kept: multiples of stride (sizes the single-pass grid)
+    int num_sms;
     int d;
     const int* rows;
     const int* nb;

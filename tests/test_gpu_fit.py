@@ -148,6 +148,25 @@ def test_bf16_fit_matches_oracle(kvb):
     _check_fit(kvb, ctx, st, pair, torch.float32, TOL_W)
 
 
+@pytest.mark.parametrize("d,H", [(32, 8), (64, 4), (16, 16)])
+def test_bf16_tensor_core_statistics_head_dims_packed_short_sequences(kvb, d, H):
+    # H*d = 256, so the statistics run on the tensor cores; the single-pass gather
+    # uses its streaming kernel for head_dim 64 and the register kernel for 16 / 32.
+    # Each batch packs 200 sequences of 1-3 tokens (positions restart at 0), so
+    # more rows are kept than T / stride and a CTA walks more than one chunk.
+    rng = np.random.default_rng(d)
+    positions = [np.concatenate([np.arange(n) for n in rng.integers(1, 4, size=200)]) for _ in range(5)]
+    pair = round_pair(make_pair(40 + d, 3, 2, H, d, 2, None, 4, 1e4, 1e6, noise=1e-2, sigma=1.0,
+                                positions=positions), torch.bfloat16)
+    ctx = _ctx(kvb, pair, 8)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, 1024)
+    kvb.kvb_profile_enable(ctx, True)
+    _accumulate(kvb, ctx, st, pair["calib"], torch.bfloat16)
+    assert "stats_gemm_tcgen05" in kvb.kvb_profile_read(ctx)
+    assert kvb.kvb_stats_count(st) == 800
+    _check_stats(kvb, st, pair, 1e-4)
+
+
 def test_bad_calibration_position_is_reported(kvb):
     pair = make_pair(13, 3, 2, 2, 16, 2, 64, 1, 1e4, 1e6)
     ctx = _ctx(kvb, pair, 32)  # positions reach 63 >= max_pos

@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(256, (R <= 4 ? 2 : 1)) gather_shift_kernel(con
 // centered values in registers, writes them as bf16 (hi, lo) runs of its
 // observations into the feature-major outputs and sums them per column: no
 // transpose through shared memory.
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)

@@ -69,7 +69,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 63u) {
+        if ((it & 7u) == 7u) {  // a failed try_wait has already suspended for a while
             if (*abort) return false;
             if (global_timer_ns() - t0 > e.timeout_ns) {
                 dev_err_set(e, DEV_ERR_TIMEOUT);

@@ -291,7 +291,7 @@ cudaError_t launch_gemm_f32(const GemmArgs& g, cudaStream_t s) {
 }
 
 cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t n, int batch, int* numeric_flag,
-                                float* Linv, int64_t strideL, cudaStream_t s) {
+                                float* Linv, int64_t strideL, const TcSolve* tc, cudaStream_t s) {
     for (int64_t k0 = 0; k0 < n; k0 += NB) {
         const int nb = static_cast<int>(n - k0 < NB ? n - k0 : NB);
         potrf_diag_kernel<<<batch, 256, 0, s>>>(G, ldg, strideG, k0, nb, numeric_flag, Linv, strideL);
@@ -317,6 +317,13 @@ cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t 
         t.batch = batch;
         cudaError_t e = launch_gemm_f32(t, s);
         if (e != cudaSuccess) return e;
+        float* trail = G + (k0 + nb) * ldg + (k0 + nb);
+        if (tc_update_supported(tc, rem, rem, nb, trail, ldg)) {  // trailing -= P P^T on the tensor cores
+            const TcOperand P{G + (k0 + nb) * ldg + k0, rem, ldg, 1, strideG};
+            e = launch_tc_update(*tc, P, nullptr, nb, trail, ldg, strideG, -1.f, 1.f, true, batch, s, nullptr);
+            if (e != cudaSuccess) return e;
+            continue;
+        }
         GemmArgs g{};
         g.A = G + (k0 + nb) * ldg + k0;  // P: rem x nb
         g.B = G + (k0 + nb) * ldg + k0;  // P^T: B(k, n) = P[n][k]
@@ -341,7 +348,7 @@ cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t 
 
 cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int64_t n, const float* Linv,
                                int64_t strideL, float* C, int64_t ldc, int64_t strideC, int64_t m, int batch,
-                               cudaStream_t s) {
+                               const TcSolve* tc, cudaStream_t s) {
     // Block row k of C times the inverse diagonal block (or its transpose), in place:
     // every output column depends only on the same column of the block row.
     auto diag = [&](int64_t k0, int nb, bool transpose) {
@@ -371,6 +378,14 @@ cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int
         if (e != cudaSuccess) return e;
         const int64_t rem = n - k0 - nb;
         if (rem <= 0) continue;
+        if (tc_update_supported(tc, rem, m, nb, C + (k0 + nb) * ldc, ldc)) {  // rows below -= L_panel Y_k
+            const TcOperand A{L + (k0 + nb) * ldg + k0, rem, ldg, 1, strideG};
+            const TcOperand Bt{C + k0 * ldc, m, 1, ldc, strideC};
+            e = launch_tc_update(*tc, A, &Bt, nb, C + (k0 + nb) * ldc, ldc, strideC, -1.f, 1.f, false, batch, s,
+                                 nullptr);
+            if (e != cudaSuccess) return e;
+            continue;
+        }
         GemmArgs g{};
         g.A = L + (k0 + nb) * ldg + k0;
         g.B = C + k0 * ldc;
@@ -398,6 +413,13 @@ cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int
         cudaError_t e = diag(k0, nb, true);
         if (e != cudaSuccess) return e;
         if (k0 == 0) break;
+        if (tc_update_supported(tc, k0, m, nb, C, ldc)) {  // rows above -= L_k^T X_k
+            const TcOperand A{L + k0 * ldg, k0, 1, ldg, strideG};
+            const TcOperand Bt{C + k0 * ldc, m, 1, ldc, strideC};
+            e = launch_tc_update(*tc, A, &Bt, nb, C, ldc, strideC, -1.f, 1.f, false, batch, s, nullptr);
+            if (e != cudaSuccess) return e;
+            continue;
+        }
         GemmArgs g{};
         g.A = L + k0 * ldg;  // A(i, kk) = L[k0 + kk][i]
         g.B = C + k0 * ldc;

@@ -50,6 +50,8 @@ struct kvb_stats {
     size_t wsS_bytes = 0;
     float* wsL = nullptr;  // inverses of the 64 x 64 diagonal blocks of the factors
     size_t wsL_bytes = 0;
+    float* wsT = nullptr;  // bf16 parts of the tensor-core update operands
+    size_t wsT_bytes = 0;
     float* r2 = nullptr;  // [2][L_t][L_s]
     int* sel = nullptr;   // [2][L_t][k]
     int* numeric = nullptr;
@@ -101,6 +103,7 @@ void free_stats(kvb_stats* st) {
     cudaFree(st->wsD);
     cudaFree(st->wsS);
     cudaFree(st->wsL);
+    cudaFree(st->wsT);
     if (st->plan) stats_gemm_tc_free(st->plan);
     delete st;
 }
@@ -424,6 +427,8 @@ kvb_status kvb_layer_select(kvb_ctx* c, kvb_stats* st, double lambda, int32_t* s
     if ((s = ws_grow(st, &st->wsS, &st->wsS_bytes, size_t(B) * Ft * 4)) != KVB_OK) return s;
     const int64_t lq = ((q + 63) / 64) * 64 * 64;  // Linv floats per system
     if ((s = ws_grow(st, &st->wsL, &st->wsL_bytes, size_t(B) * lq * 4)) != KVB_OK) return s;
+    if ((s = ws_grow(st, &st->wsT, &st->wsT_bytes, tc_update_ws_bytes(q, Ft, B))) != KVB_OK) return s;
+    const TcSolve tc{reinterpret_cast<__nv_bfloat16*>(st->wsT), st->wsT_bytes, dev_err(c), c->num_sms};
     cudaError_t e = cudaMemsetAsync(st->numeric, 0, sizeof(int), cs);
     const float lam = static_cast<float>(lambda);
     {
@@ -438,10 +443,10 @@ kvb_status kvb_layer_select(kvb_ctx* c, kvb_stats* st, double lambda, int32_t* s
                 if (e == cudaSuccess)
                     e = launch_gather_rhs(st->cross[kv], Ft, L, q, q, Ft, st->wsD, st->wsR, int64_t(q) * Ft, nb, cs);
                 if (e == cudaSuccess)
-                    e = chol_factor_batched(st->wsG, q, int64_t(q) * q, q, nb, st->numeric, st->wsL, lq, cs);
+                    e = chol_factor_batched(st->wsG, q, int64_t(q) * q, q, nb, st->numeric, st->wsL, lq, &tc, cs);
                 if (e == cudaSuccess)
                     e = chol_solve_batched(st->wsG, q, int64_t(q) * q, q, st->wsL, lq, st->wsR, Ft, int64_t(q) * Ft, Ft,
-                                           nb, cs);
+                                           nb, &tc, cs);
                 if (e == cudaSuccess)
                     e = launch_sse(st->cross[kv], Ft, L, q, q, Ft, st->wsD, st->wsR, int64_t(q) * Ft, st->syy[kv], lam,
                                    st->wsS, nb, cs);
@@ -495,6 +500,8 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
     if ((s = ws_grow(st, &st->wsD, &st->wsD_bytes, size_t(B) * p * 4)) != KVB_OK) return s;
     const int64_t lp = ((p + 63) / 64) * 64 * 64;  // Linv floats per system
     if ((s = ws_grow(st, &st->wsL, &st->wsL_bytes, size_t(B) * lp * 4)) != KVB_OK) return s;
+    if ((s = ws_grow(st, &st->wsT, &st->wsT_bytes, tc_update_ws_bytes(p, q, B))) != KVB_OK) return s;
+    const TcSolve tc{reinterpret_cast<__nv_bfloat16*>(st->wsT), st->wsT_bytes, dev_err(c), c->num_sms};
     cudaError_t e = cudaMemsetAsync(st->numeric, 0, sizeof(int), cs);
     const float lam = static_cast<float>(lambda);
     void* Wout[2] = {W_k, W_v};
@@ -518,9 +525,10 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
                 }
                 e = launch_gather_system(st->gram[kv], st->Fs, L, q, p, lam, st->wsG, p * p, st->wsD, nb, cs);
                 if (e == cudaSuccess) e = launch_gather_rhs(st->cross[kv], st->Ft, L, q, p, q, st->wsD, st->wsR, p * q, nb, cs);
-                if (e == cudaSuccess) e = chol_factor_batched(st->wsG, p, p * p, p, nb, st->numeric, st->wsL, lp, cs);
                 if (e == cudaSuccess)
-                    e = chol_solve_batched(st->wsG, p, p * p, p, st->wsL, lp, st->wsR, q, p * q, q, nb, cs);
+                    e = chol_factor_batched(st->wsG, p, p * p, p, nb, st->numeric, st->wsL, lp, &tc, cs);
+                if (e == cudaSuccess)
+                    e = chol_solve_batched(st->wsG, p, p * p, p, st->wsL, lp, st->wsR, q, p * q, q, nb, &tc, cs);
                 if (e == cudaSuccess) e = launch_write_w(w_dtype, st->wsR, p * q, st->wsD, p, q, O, nb, cs);
                 if (e == cudaSuccess)
                     e = launch_bias(st->wsR, p * q, st->wsD, p, q, L, q, st->mean[kv], st->mean[2 + kv], O, nb, cs);

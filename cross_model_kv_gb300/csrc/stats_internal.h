@@ -1,6 +1,8 @@
 // Internal declarations of the statistics, selection and ridge-solve kernels.
 #pragma once
 
+#include <string>
+
 #include "kvb_internal.h"
 
 namespace kvb {
@@ -104,10 +106,31 @@ cudaError_t launch_gemm_f32(const GemmArgs& g, cudaStream_t s);
 // also leaves the inverse of every 64 x 64 diagonal block in Linv
 // ([batch][n/64 * 64][64], strideL floats per system), so both triangular
 // solves run as GEMMs.  A non-positive pivot sets *numeric_flag.
+// Rank-64 updates on the tensor cores with fp32 operands carried as three bf16
+// parts (solve_tc_sm103.cu).  An operand is rows x K (K <= 64) fp32 with
+// element (r, k) of batch item b at src[b * s_batch + r * s_row + k * s_k].
+struct TcOperand {
+    const float* src;
+    int64_t rows, s_row, s_k, s_batch;
+};
+struct TcSolve {
+    __nv_bfloat16* ws;  // split operands, tc_update_ws_bytes()
+    size_t ws_bytes;
+    DevErr err;
+    int num_sms;
+};
+size_t tc_update_ws_bytes(int64_t rows_a, int64_t rows_b, int batch);
+bool tc_update_supported(const TcSolve* tc, int64_t M, int64_t N, int K, const float* C, int64_t ldc);
+// C[b] = alpha * A[b] B[b]^T + beta * C[b] (B == NULL: B = A); lower skips tiles above the diagonal.
+cudaError_t launch_tc_update(const TcSolve& tc, const TcOperand& A, const TcOperand* B, int K, float* C, int64_t ldc,
+                             int64_t strideC, float alpha, float beta, bool lower, int batch, cudaStream_t s,
+                             std::string* why);
+
+// tc (may be NULL): run the large rank-64 updates on the tensor cores.
 cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t n, int batch, int* numeric_flag,
-                                float* Linv, int64_t strideL, cudaStream_t s);
+                                float* Linv, int64_t strideL, const TcSolve* tc, cudaStream_t s);
 cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int64_t n, const float* Linv,
                                int64_t strideL, float* C, int64_t ldc, int64_t strideC, int64_t m, int batch,
-                               cudaStream_t s);
+                               const TcSolve* tc, cudaStream_t s);
 
 }  // namespace kvb

@@ -290,57 +290,80 @@ cudaError_t launch_gemm_f32(const GemmArgs& g, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+namespace {
+
+// C[b] = alpha * A[b] B[b]^T + beta * C[b] over a batch of systems, A (M x K)
+// and B (N x K) fp32 with element (r, k) at src[r * s_row + k * s_k]: on the
+// tensor cores when the update is large, otherwise on the CUDA cores.
+cudaError_t update(const TcSolve* tc, const float* A, int64_t a_row, int64_t a_k, int64_t strideA, int64_t M,
+                   const float* B, int64_t b_row, int64_t b_k, int64_t strideB, int64_t N, int K, float* C,
+                   int64_t ldc, int64_t strideC, float alpha, float beta, bool lower, int batch, cudaStream_t s) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    if (tc_update_supported(tc, M, N, K, C, ldc)) {
+        const TcOperand a{A, M, a_row, a_k, strideA};
+        if (A == B && a_row == b_row && a_k == b_k && M == N)
+            return launch_tc_update(*tc, a, nullptr, K, C, ldc, strideC, alpha, beta, lower, batch, s, nullptr);
+        const TcOperand b{B, N, b_row, b_k, strideB};
+        return launch_tc_update(*tc, a, &b, K, C, ldc, strideC, alpha, beta, lower, batch, s, nullptr);
+    }
+    GemmArgs g{};
+    g.A = A;
+    g.sam = a_row;
+    g.sak = a_k;
+    g.B = B;  // B(k, n) = B[n * b_row + k * b_k]
+    g.sbk = b_k;
+    g.sbn = b_row;
+    g.C = C;
+    g.ldc = ldc;
+    g.strideA = strideA;
+    g.strideB = strideB;
+    g.strideC = strideC;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.alpha = alpha;
+    g.beta = beta;
+    g.batch = batch;
+    g.lower = lower ? 1 : 0;
+    return launch_gemm_f32(g, s);
+}
+
+}  // namespace
+
+// Right-looking blocked Cholesky with 128-wide super-panels: the two 64-wide
+// halves are factored one after the other (the second half's columns updated
+// by the first half's panel alone), then the trailing matrix takes one
+// rank-128 update, which halves its read-modify-write passes against 64-wide
+// steps.
 cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t n, int batch, int* numeric_flag,
                                 float* Linv, int64_t strideL, const TcSolve* tc, cudaStream_t s) {
-    for (int64_t k0 = 0; k0 < n; k0 += NB) {
-        const int nb = static_cast<int>(n - k0 < NB ? n - k0 : NB);
-        potrf_diag_kernel<<<batch, 256, 0, s>>>(G, ldg, strideG, k0, nb, numeric_flag, Linv, strideL);
-        const int64_t rem = n - k0 - nb;
-        if (rem <= 0) continue;
-        // panel below the diagonal block: P <- P L_kk^-T (rows independent, in place)
-        GemmArgs t{};
-        t.A = G + (k0 + nb) * ldg + k0;
-        t.B = Linv + k0 * NB;  // B(k, n) = Linv[n][k]
-        t.C = G + (k0 + nb) * ldg + k0;
-        t.sam = ldg;
-        t.sak = 1;
-        t.sbk = 1;
-        t.sbn = NB;
-        t.ldc = ldg;
-        t.strideA = t.strideC = strideG;
-        t.strideB = strideL;
-        t.M = rem;
-        t.N = nb;
-        t.K = nb;
-        t.alpha = 1.f;
-        t.beta = 0.f;
-        t.batch = batch;
-        cudaError_t e = launch_gemm_f32(t, s);
-        if (e != cudaSuccess) return e;
-        float* trail = G + (k0 + nb) * ldg + (k0 + nb);
-        if (tc_update_supported(tc, rem, rem, nb, trail, ldg)) {  // trailing -= P P^T on the tensor cores
-            const TcOperand P{G + (k0 + nb) * ldg + k0, rem, ldg, 1, strideG};
-            e = launch_tc_update(*tc, P, nullptr, nb, trail, ldg, strideG, -1.f, 1.f, true, batch, s, nullptr);
+    cudaError_t e = cudaSuccess;
+    for (int64_t k0 = 0; k0 < n; k0 += 2 * NB) {
+        for (int half = 0; half < 2; ++half) {
+            const int64_t j0 = k0 + half * NB;  // first column of this 64-wide half
+            if (j0 >= n) break;
+            const int nb = static_cast<int>(n - j0 < NB ? n - j0 : NB);
+            potrf_diag_kernel<<<batch, 256, 0, s>>>(G, ldg, strideG, j0, nb, numeric_flag, Linv, strideL);
+            const int64_t rem = n - j0 - nb;
+            if (rem <= 0) break;
+            // panel below the diagonal block: P <- P L_jj^-T (rows independent, in place);
+            // B(k, n) = Linv[n][k]
+            e = update(nullptr, G + (j0 + nb) * ldg + j0, ldg, 1, strideG, rem, Linv + j0 * NB, NB, 1, strideL, nb,
+                       nb, G + (j0 + nb) * ldg + j0, ldg, strideG, 1.f, 0.f, false, batch, s);
             if (e != cudaSuccess) return e;
-            continue;
+            if (half == 0 && rem > 0) {  // the second half's columns, rows below the first half
+                const int nb2 = static_cast<int>(rem < NB ? rem : NB);
+                const float* P1 = G + (j0 + nb) * ldg + j0;
+                e = update(nullptr, P1, ldg, 1, strideG, rem, P1, ldg, 1, strideG, nb2, nb,
+                           G + (j0 + nb) * ldg + (j0 + nb), ldg, strideG, -1.f, 1.f, false, batch, s);
+                if (e != cudaSuccess) return e;
+            }
         }
-        GemmArgs g{};
-        g.A = G + (k0 + nb) * ldg + k0;  // P: rem x nb
-        g.B = G + (k0 + nb) * ldg + k0;  // P^T: B(k, n) = P[n][k]
-        g.C = G + (k0 + nb) * ldg + (k0 + nb);
-        g.sam = ldg;
-        g.sak = 1;
-        g.sbk = 1;
-        g.sbn = ldg;
-        g.ldc = ldg;
-        g.strideA = g.strideB = g.strideC = strideG;
-        g.M = g.N = rem;
-        g.K = nb;
-        g.alpha = -1.f;
-        g.beta = 1.f;
-        g.batch = batch;
-        g.lower = 1;
-        e = launch_gemm_f32(g, s);
+        const int64_t t0 = k0 + 2 * NB;  // trailing matrix of the super-panel
+        if (t0 >= n) break;
+        const float* P = G + t0 * ldg + k0;  // (n - t0) x 128
+        e = update(tc, P, ldg, 1, strideG, n - t0, P, ldg, 1, strideG, n - t0, 2 * NB, G + t0 * ldg + t0, ldg,
+                   strideG, -1.f, 1.f, true, batch, s);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
@@ -349,13 +372,13 @@ cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t 
 cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int64_t n, const float* Linv,
                                int64_t strideL, float* C, int64_t ldc, int64_t strideC, int64_t m, int batch,
                                const TcSolve* tc, cudaStream_t s) {
-    // Block row k of C times the inverse diagonal block (or its transpose), in place:
+    // Block row j of C times the inverse diagonal block (or its transpose), in place:
     // every output column depends only on the same column of the block row.
-    auto diag = [&](int64_t k0, int nb, bool transpose) {
+    auto diag = [&](int64_t j0, int nb, bool transpose) {
         GemmArgs t{};
-        t.A = Linv + k0 * NB;
-        t.B = C + k0 * ldc;
-        t.C = C + k0 * ldc;
+        t.A = Linv + j0 * NB;
+        t.B = C + j0 * ldc;
+        t.C = C + j0 * ldc;
         t.sam = transpose ? 1 : NB;
         t.sak = transpose ? NB : 1;
         t.sbk = ldc;
@@ -371,73 +394,44 @@ cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int
         t.batch = batch;
         return launch_gemm_f32(t, s);
     };
-    // forward: L Y = C
-    for (int64_t k0 = 0; k0 < n; k0 += NB) {
-        const int nb = static_cast<int>(n - k0 < NB ? n - k0 : NB);
-        cudaError_t e = diag(k0, nb, false);
-        if (e != cudaSuccess) return e;
-        const int64_t rem = n - k0 - nb;
-        if (rem <= 0) continue;
-        if (tc_update_supported(tc, rem, m, nb, C + (k0 + nb) * ldc, ldc)) {  // rows below -= L_panel Y_k
-            const TcOperand A{L + (k0 + nb) * ldg + k0, rem, ldg, 1, strideG};
-            const TcOperand Bt{C + k0 * ldc, m, 1, ldc, strideC};
-            e = launch_tc_update(*tc, A, &Bt, nb, C + (k0 + nb) * ldc, ldc, strideC, -1.f, 1.f, false, batch, s,
-                                 nullptr);
+    cudaError_t e;
+    // forward, L Y = C, 128 rows at a time: Y1 = L11^-1 C1; C2 -= L21 Y1; Y2 = L22^-1 C2;
+    // then one rank-128 update of every row below
+    for (int64_t k0 = 0; k0 < n; k0 += 2 * NB) {
+        const int nb1 = static_cast<int>(n - k0 < NB ? n - k0 : NB);
+        const int nb2 = static_cast<int>(n - k0 - nb1 <= 0 ? 0 : (n - k0 - nb1 < NB ? n - k0 - nb1 : NB));
+        if ((e = diag(k0, nb1, false)) != cudaSuccess) return e;
+        if (nb2 > 0) {
+            // B(k, n) = C[k0 + k][n]: row stride 1, k stride ldc
+            e = update(nullptr, L + (k0 + NB) * ldg + k0, ldg, 1, strideG, nb2, C + k0 * ldc, 1, ldc, strideC, m,
+                       nb1, C + (k0 + NB) * ldc, ldc, strideC, -1.f, 1.f, false, batch, s);
             if (e != cudaSuccess) return e;
-            continue;
+            if ((e = diag(k0 + NB, nb2, false)) != cudaSuccess) return e;
         }
-        GemmArgs g{};
-        g.A = L + (k0 + nb) * ldg + k0;
-        g.B = C + k0 * ldc;
-        g.C = C + (k0 + nb) * ldc;
-        g.sam = ldg;
-        g.sak = 1;
-        g.sbk = ldc;
-        g.sbn = 1;
-        g.ldc = ldc;
-        g.strideA = strideG;
-        g.strideB = g.strideC = strideC;
-        g.M = rem;
-        g.N = m;
-        g.K = nb;
-        g.alpha = -1.f;
-        g.beta = 1.f;
-        g.batch = batch;
-        e = launch_gemm_f32(g, s);
+        const int64_t t0 = k0 + nb1 + nb2;
+        if (t0 >= n) break;
+        e = update(tc, L + t0 * ldg + k0, ldg, 1, strideG, n - t0, C + k0 * ldc, 1, ldc, strideC, m, nb1 + nb2,
+                   C + t0 * ldc, ldc, strideC, -1.f, 1.f, false, batch, s);
         if (e != cudaSuccess) return e;
     }
-    // backward: L^T X = Y
-    const int64_t last = ((n - 1) / NB) * NB;
-    for (int64_t k0 = last; k0 >= 0; k0 -= NB) {
-        const int nb = static_cast<int>(n - k0 < NB ? n - k0 : NB);
-        cudaError_t e = diag(k0, nb, true);
-        if (e != cudaSuccess) return e;
-        if (k0 == 0) break;
-        if (tc_update_supported(tc, k0, m, nb, C, ldc)) {  // rows above -= L_k^T X_k
-            const TcOperand A{L + k0 * ldg, k0, 1, ldg, strideG};
-            const TcOperand Bt{C + k0 * ldc, m, 1, ldc, strideC};
-            e = launch_tc_update(*tc, A, &Bt, nb, C, ldc, strideC, -1.f, 1.f, false, batch, s, nullptr);
+    // backward, L^T X = Y, last super-block first: X2 = L22^-T Y2; Y1 -= L21^T X2;
+    // X1 = L11^-T Y1; then one rank-128 update of every row above
+    const int64_t last = ((n - 1) / (2 * NB)) * (2 * NB);
+    for (int64_t k0 = last; k0 >= 0; k0 -= 2 * NB) {
+        const int nb1 = static_cast<int>(n - k0 < NB ? n - k0 : NB);
+        const int nb2 = static_cast<int>(n - k0 - nb1 <= 0 ? 0 : (n - k0 - nb1 < NB ? n - k0 - nb1 : NB));
+        if (nb2 > 0) {
+            if ((e = diag(k0 + NB, nb2, true)) != cudaSuccess) return e;
+            // A(i, kk) = L[k0 + NB + kk][k0 + i]: row stride 1, k stride ldg
+            e = update(nullptr, L + (k0 + NB) * ldg + k0, 1, ldg, strideG, nb1, C + (k0 + NB) * ldc, 1, ldc, strideC,
+                       m, nb2, C + k0 * ldc, ldc, strideC, -1.f, 1.f, false, batch, s);
             if (e != cudaSuccess) return e;
-            continue;
         }
-        GemmArgs g{};
-        g.A = L + k0 * ldg;  // A(i, kk) = L[k0 + kk][i]
-        g.B = C + k0 * ldc;
-        g.C = C;
-        g.sam = 1;
-        g.sak = ldg;
-        g.sbk = ldc;
-        g.sbn = 1;
-        g.ldc = ldc;
-        g.strideA = strideG;
-        g.strideB = g.strideC = strideC;
-        g.M = k0;
-        g.N = m;
-        g.K = nb;
-        g.alpha = -1.f;
-        g.beta = 1.f;
-        g.batch = batch;
-        e = launch_gemm_f32(g, s);
+        if ((e = diag(k0, nb1, true)) != cudaSuccess) return e;
+        if (k0 == 0) break;
+        // rows above: A(i, kk) = L[k0 + kk][i] for i < k0
+        e = update(tc, L + k0 * ldg, 1, ldg, strideG, k0, C + k0 * ldc, 1, ldc, strideC, m, nb1 + nb2, C, ldc,
+                   strideC, -1.f, 1.f, false, batch, s);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

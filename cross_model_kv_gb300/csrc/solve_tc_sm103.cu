@@ -3,8 +3,8 @@
 //
 // The ridge systems of the fit ("KVBridge" README, "Loading": W = (M +
 // lambda I)^-1 C) and of the single-source R^2 ("What ships") are solved in
-// float32 by a blocked Cholesky whose work is rank-64 updates
-//     C = alpha * A B^T + beta * C      (A: M x 64, B: N x 64, C fp32)
+// float32 by a blocked Cholesky whose work is rank-128 (and rank-64) updates
+//     C = alpha * A B^T + beta * C      (A: M x K, B: N x K, K <= 128, C fp32)
 // of the trailing matrix and of the right-hand sides.  Here every fp32
 // operand x is carried as three bf16 parts, x1 = bf16(x), x2 = bf16(x - x1),
 // x3 = bf16(x - x1 - x2) (24 significant bits in all), and the product is
@@ -31,7 +31,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 64;  // one 128-byte swizzle atom of bf16; the update rank
+constexpr int BK = 64;  // one 128-byte swizzle atom of bf16
+constexpr int KMAX = 128;  // largest update rank
 constexpr int STAGES = 2;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
@@ -48,7 +49,7 @@ __constant__ int kPartB[NPROD] = {0, 1, 0, 2, 1, 0};
 struct Params {
     float* C;
     int64_t ldc, strideC;
-    int M, N, lower;
+    int M, N, lower, nkb;  // nkb: 64-wide K blocks (1 or 2)
     float alpha, beta;
     DevErr err;
 };
@@ -104,11 +105,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 2) solve_gemm_kernel(const __grid
             for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
             uint32_t phase = 0;
             int stage = 0;
-            for (int pr = 0; pr < NPROD; ++pr) {
+            for (int it = 0; it < P.nkb * NPROD; ++it) {
+                const int kb = it / NPROD, pr = it - kb * NPROD;
                 if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) break;
                 mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                tma_load_3d(sA + stage * A_BYTES, &Mp.a[kPartA[pr]], &full[stage], 0, m0, bz);
-                tma_load_3d(sB + stage * B_BYTES, &Mp.b[kPartB[pr]], &full[stage], 0, n0, bz);
+                tma_load_3d(sA + stage * A_BYTES, &Mp.a[kPartA[pr]], &full[stage], kb * BK, m0, bz);
+                tma_load_3d(sB + stage * B_BYTES, &Mp.b[kPartB[pr]], &full[stage], kb * BK, n0, bz);
                 issued_phase[stage] = static_cast<int>(phase);
                 if (++stage == STAGES) {
                     stage = 0;
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2) solve_gemm_kernel(const __grid
             uint32_t phase = 0;
             int stage = 0;
             bool ok = true;
-            for (int pr = 0; pr < NPROD; ++pr) {
+            for (int it = 0; it < P.nkb * NPROD; ++it) {
                 if (!mbar_wait(&full[stage], phase, P.err, abort_flag)) {
                     ok = false;
                     break;
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2) solve_gemm_kernel(const __grid
                 const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
-                    umma_bf16(tmem_base, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc, (pr | k) != 0);
+                    umma_bf16(tmem_base, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc, (it | k) != 0);
                 umma_commit(&empty[stage]);
                 if (++stage == STAGES) {
                     stage = 0;
@@ -151,7 +153,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 2) solve_gemm_kernel(const __grid
     } else {
         // ----------------------------------------------------------- epilogue
         const int sub = warp & 3;  // TMEM lane quarter this warp may access
-        const int row = m0 + sub * 32 + lane;
         if (mbar_wait(tfull, 0, P.err, abort_flag)) {
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16);
@@ -213,11 +214,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 2) solve_gemm_kernel(const __grid
     }
 }
 
-// Three bf16 parts of a rows x K fp32 operand (K <= 64), written K-major as
-// [batch][rows][64] with zeros beyond K.  Element (r, k) of batch item b is
+// Three bf16 parts of a rows x K fp32 operand (K <= kp), written K-major as
+// [batch][rows][kp] with zeros beyond K.  Element (r, k) of batch item b is
 // src[b * s_batch + r * s_row + k * s_k]; 32 x 32 tiles through shared
 // memory so that both K-contiguous and row-contiguous sources read coalesced.
-__global__ void __launch_bounds__(256) split3_kernel(const float* __restrict__ src, int64_t rows, int K,
+__global__ void __launch_bounds__(256) split3_kernel(const float* __restrict__ src, int64_t rows, int K, int kp,
                                                      int64_t s_row, int64_t s_k, int64_t s_batch,
                                                      __nv_bfloat16* __restrict__ p0, __nv_bfloat16* __restrict__ p1,
                                                      __nv_bfloat16* __restrict__ p2) {
@@ -252,21 +253,22 @@ __global__ void __launch_bounds__(256) split3_kernel(const float* __restrict__ s
         const float e1 = x - __bfloat162float(x1);
         const __nv_bfloat16 x2 = __float2bfloat16_rn(e1);
         const __nv_bfloat16 x3 = __float2bfloat16_rn(e1 - __bfloat162float(x2));
-        const int64_t o = (static_cast<int64_t>(b) * rows + r) * BK + k0 + tx;
+        const int64_t o = (static_cast<int64_t>(b) * rows + r) * kp + k0 + tx;
         p0[o] = x1;
         p1[o] = x2;
         p2[o] = x3;
     }
 }
 
-bool encode_parts(CUtensorMap* m, const void* base, int64_t rows, int batch, uint32_t box_rows, std::string* why) {
+bool encode_parts(CUtensorMap* m, const void* base, int64_t rows, int batch, int kp, uint32_t box_rows,
+                  std::string* why) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) {
         if (why) *why = "cuTensorMapEncodeTiled unavailable from the driver";
         return false;
     }
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(batch)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(BK) * 2, static_cast<cuuint64_t>(rows) * BK * 2};
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kp), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kp) * 2, static_cast<cuuint64_t>(rows) * kp * 2};
     cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -279,21 +281,22 @@ bool encode_parts(CUtensorMap* m, const void* base, int64_t rows, int batch, uin
     return true;
 }
 
-cudaError_t split3(const TcOperand& o, int K, int batch, __nv_bfloat16* dst, cudaStream_t s) {
-    const int64_t part = static_cast<int64_t>(batch) * o.rows * BK;
-    dim3 grid(static_cast<unsigned>((o.rows + 31) / 32), BK / 32, static_cast<unsigned>(batch));
-    split3_kernel<<<grid, 256, 0, s>>>(o.src, o.rows, K, o.s_row, o.s_k, o.s_batch, dst, dst + part, dst + 2 * part);
+cudaError_t split3(const TcOperand& o, int K, int kp, int batch, __nv_bfloat16* dst, cudaStream_t s) {
+    const int64_t part = static_cast<int64_t>(batch) * o.rows * kp;
+    dim3 grid(static_cast<unsigned>((o.rows + 31) / 32), static_cast<unsigned>(kp / 32), static_cast<unsigned>(batch));
+    split3_kernel<<<grid, 256, 0, s>>>(o.src, o.rows, K, kp, o.s_row, o.s_k, o.s_batch, dst, dst + part,
+                                       dst + 2 * part);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t tc_update_ws_bytes(int64_t rows_a, int64_t rows_b, int batch) {
-    return 3ull * static_cast<size_t>(batch) * static_cast<size_t>(rows_a + rows_b) * BK * 2 + 1024;
+    return 3ull * static_cast<size_t>(batch) * static_cast<size_t>(rows_a + rows_b) * KMAX * 2 + 1024;
 }
 
 bool tc_update_supported(const TcSolve* tc, int64_t M, int64_t N, int K, const float* C, int64_t ldc) {
-    return tc && tc->ws && tc->num_sms > 0 && K <= BK && M >= 256 && N >= 256 && N % 16 == 0 && ldc % 4 == 0 &&
+    return tc && tc->ws && tc->num_sms > 0 && K >= 1 && K <= KMAX && M >= 256 && N >= 256 && N % 16 == 0 && ldc % 4 == 0 &&
            (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && M <= 0x7fffffffLL && N <= 0x7fffffffLL;
 }
 
@@ -305,17 +308,18 @@ cudaError_t launch_tc_update(const TcSolve& tc, const TcOperand& A, const TcOper
         if (why) *why = "tensor-core update workspace too small";
         return cudaErrorInvalidValue;
     }
+    const int kp = K <= BK ? BK : KMAX;
     __nv_bfloat16* wa = tc.ws;
-    __nv_bfloat16* wb = wa + 3 * static_cast<int64_t>(batch) * A.rows * BK;
-    cudaError_t e = split3(A, K, batch, wa, s);
-    if (e == cudaSuccess && B) e = split3(*B, K, batch, wb, s);
+    __nv_bfloat16* wb = wa + 3 * static_cast<int64_t>(batch) * A.rows * kp;
+    cudaError_t e = split3(A, K, kp, batch, wa, s);
+    if (e == cudaSuccess && B) e = split3(*B, K, kp, batch, wb, s);
     if (e != cudaSuccess) return e;
     const int64_t N = B ? B->rows : A.rows;
     const __nv_bfloat16* bb = B ? wb : wa;
     Maps mp;
     for (int i = 0; i < 3; ++i) {
-        if (!encode_parts(&mp.a[i], wa + i * static_cast<int64_t>(batch) * A.rows * BK, A.rows, batch, BM, why) ||
-            !encode_parts(&mp.b[i], bb + i * static_cast<int64_t>(batch) * N * BK, N, batch, BN, why))
+        if (!encode_parts(&mp.a[i], wa + i * static_cast<int64_t>(batch) * A.rows * kp, A.rows, batch, kp, BM, why) ||
+            !encode_parts(&mp.b[i], bb + i * static_cast<int64_t>(batch) * N * kp, N, batch, kp, BN, why))
             return cudaErrorInvalidValue;
     }
     Params P{};
@@ -325,6 +329,7 @@ cudaError_t launch_tc_update(const TcSolve& tc, const TcOperand& A, const TcOper
     P.M = static_cast<int>(A.rows);
     P.N = static_cast<int>(N);
     P.lower = lower ? 1 : 0;
+    P.nkb = kp / BK;
     P.alpha = alpha;
     P.beta = beta;
     P.err = tc.err;

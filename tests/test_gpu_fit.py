@@ -106,6 +106,18 @@ def test_tiny_pair_fp32_fit_matches_oracle_and_recovers(kvb):
             assert O.head_pooled_r2(A, B, 2, 16) > 0.9999
 
 
+def test_fp32_fit_system_size_not_a_multiple_of_the_panels(kvb):
+    # head_dim 24, 4 KV heads, k = 5: ridge systems of 480 unknowns (7.5 panels of 64,
+    # a partial last 128-wide super-panel) whose large trailing updates run on the
+    # tensor cores; 8 sequences x 512 tokens, stride 4 -> 1024 observations
+    pair = make_pair(5, 5, 2, 4, 24, 5, 512, 8, 1e4, 1e6)
+    ctx = _ctx(kvb, pair, 512)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 512)
+    _accumulate(kvb, ctx, st, pair["calib"], torch.float32)
+    assert kvb.kvb_stats_count(st) == 1024
+    _check_fit(kvb, ctx, st, pair, torch.float32, 1e-4)
+
+
 def test_chan_merge_over_ragged_batches_and_offsets(kvb):
     # unequal batch lengths, positions not starting at 0: merges must equal two-pass statistics
     rng = np.random.default_rng(3)

@@ -410,12 +410,14 @@ def run_attention(kvb, dev, seed=301):
     kvb.kvb_profile_enable(ctx, False)
     kvb.kvb_ctx_check(ctx, stream)
     ms = e0.elapsed_time(e1) / reps
-    n, kern_ms = kvb.kvb_profile_read(ctx).get("attention_cosine", (0, 0.0))
+    prof = kvb.kvb_profile_read(ctx)
+    kname = "attention_cosine_tcgen05" if "attention_cosine_tcgen05" in prof else "attention_cosine"
+    n, kern_ms = prof.get(kname, (0, 0.0))
     flop = A["n_seq"] * (T * (T + 1) // 2) * L * Hq * 4 * d * 2
     cos = out.double()
     res = {"workload": f"qwen3-32b target geometry ({L} layers, {Hq} query / {H} KV heads, d={d}): "
                        f"{A['n_seq']} held-out sequences x {T} tokens, all positions queried, bf16 caches",
-           "ms_per_pass": ms, "kernel": "attention_cosine", "launches_per_pass": n // reps,
+           "ms_per_pass": ms, "kernel": kname, "launches_per_pass": n // reps,
            "avg_launch_ms": kern_ms / max(n, 1), "algorithmic_flop_per_pass": flop,
            "achieved_tflops": flop / (kern_ms / reps / 1e3) / 1e12 if kern_ms else None,
            "cos_mean": float(cos.mean()), "cos_min": float(cos.min()),
@@ -427,16 +429,24 @@ def run_attention(kvb, dev, seed=301):
 
 
 def attn_roofline(attn, clk):
-    """Roofline of the attention-cosine kernel: fp32 FMA on CUDA cores.
+    """Roofline of the attention-cosine kernel.
 
-    Peak = SMs x 128 fp32 lanes x 2 flop x the maximum SM clock that the
-    sampler read (2070 MHz when it read none).
+    Tensor-core kernel: against the measured bf16 burst peak (the diagnostic
+    runs briefly, alone).  CUDA-core kernel: fp32 FMA, peak = SMs x 128 fp32
+    lanes x 2 flop x the maximum SM clock that the sampler read (2070 MHz when
+    it read none).
     """
     if attn is None:
         return None
+    a = attn.get("achieved_tflops")
+    if attn["kernel"].endswith("tcgen05"):
+        peaks, kind = measured_peaks()
+        peak = peaks["bf16_tflops"]
+        return dict(attn, roofline={"bound": "tensor", "achieved": a, "peak": peak, "unit": "TFLOP/s",
+                                    "frac": a / peak if a else None,
+                                    "peak_kind": f"{kind} bf16 burst; algorithmic flops (visible pairs only)"})
     mhz = (clk or {}).get("sm_max_mhz") or 2070.0
     peak = attn["sm_count"] * 128 * 2 * mhz * 1e6 / 1e12
-    a = attn.get("achieved_tflops")
     return dict(attn, roofline={"bound": "alu", "achieved": a, "peak": peak, "unit": "TFLOP/s",
                                 "frac": a / peak if a else None,
                                 "peak_kind": f"derived: {attn['sm_count']} SMs x 128 fp32 lanes x 2 flop x {mhz:.0f} MHz"})

@@ -318,6 +318,20 @@ extern "C" kvb_status kvb_attention_cosine(kvb_ctx* c, kvb_dtype dtype, const vo
     P.scale = 1.f / sqrtf(static_cast<float>(d));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    if (attn_tc_supported(dtype, d, T) && T <= 0x7fffffffLL) {
+        std::string why;
+        {
+            ProfScope ps(c, s, "attention_cosine_tcgen05");
+            e = launch_attn_cosine_tc(q, q_pos, k_a, v_a, k_b, v_b, kv_pos, cos_out, c->L_t, c->H, n_q_heads,
+                                      static_cast<int>(Tq), T, dev_err(c), s, &why);
+        }
+        if (e != cudaSuccess) {
+            if (!why.empty()) return fail(KVB_ERR_CUDA, "attention cosine launch: " + why);
+            return cuda_fail(e, "attention cosine launch");
+        }
+        mirror_device_error(c, s);
+        return KVB_OK;
+    }
     ProfScope ps(c, s, "attention_cosine");
     const bool bf = dtype == KVB_BF16;
     switch (d) {

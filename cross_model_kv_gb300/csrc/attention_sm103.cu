@@ -40,7 +40,7 @@ constexpr int ATOM = 128 * 128;         // bytes of a 128-row x 64-element bf16 
 constexpr int TILE = 2 * ATOM;          // 128 x 128 bf16
 constexpr int NUM_THREADS = 192;
 constexpr int MAX_FLAG_TILES = 1024;
-constexpr int SMEM_BYTES = 6 * TILE + 1024 + 256 + MAX_FLAG_TILES;
+constexpr int SMEM_BYTES = 6 * TILE + 1024 + 256 + MAX_FLAG_TILES + 4 * TK * 4;
 constexpr uint64_t DRAIN_NS = 200ull * 1000 * 1000;
 constexpr uint32_t COL_S = 0, COL_OT = 128, COL_O = 256;  // O of cache x at COL_O + 128 x
 
@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* qmax_s = reinterpret_cast<int*>(tmem_slot + 2);
     uint8_t* flags = reinterpret_cast<uint8_t*>(bar) + 256;
+    int* wpos = reinterpret_cast<int*>(flags + MAX_FLAG_TILES);  // per softmax warp: the tile's key positions
 
     const int g = P.Hq / P.H;
     const int rows = g * P.Tq;
@@ -234,70 +235,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int t = 0; t < ntiles; ++t) {
                 if (!live(t)) continue;
                 const int j0 = t * TK;
-                if (!wait_all(s_full, it & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // pass 1: the row's largest visible score of the tile
-                float mt = -INFINITY;
-#pragma unroll 1
-                for (int c0 = 0; c0 < TK; c0 += 16) {
-                    uint32_t sv[16];
-                    tmem_ld16(tl + COL_S + c0, sv);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int u = 0; u < 16; u += 4) {
-                        const int j = j0 + c0 + u;
-                        int4 kp = make_int4(INT_MAX, INT_MAX, INT_MAX, INT_MAX);
-                        if (j + 3 < P.T) {
-                            kp = make_int4(__ldg(P.kv_pos + j), __ldg(P.kv_pos + j + 1), __ldg(P.kv_pos + j + 2),
-                                           __ldg(P.kv_pos + j + 3));
-                        } else {
-                            if (j < P.T) kp.x = __ldg(P.kv_pos + j);
-                            if (j + 1 < P.T) kp.y = __ldg(P.kv_pos + j + 1);
-                            if (j + 2 < P.T) kp.z = __ldg(P.kv_pos + j + 2);
-                        }
-                        const int kpa[4] = {kp.x, kp.y, kp.z, kp.w};
-#pragma unroll
-                        for (int w = 0; w < 4; ++w)
-                            if (valid && j + w < P.T && kpa[w] <= qp)
-                                mt = fmaxf(mt, __uint_as_float(sv[u + w]) * P.scale_log2);
-                    }
-                }
-                const float m_new = fmaxf(m, mt);
-                const float alpha = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
-                // pass 2: probabilities as bf16 (hi, lo) in the operand layout
-#pragma unroll 1
-                for (int c0 = 0; c0 < TK; c0 += 16) {
-                    uint32_t sv[16];
-                    tmem_ld16(tl + COL_S + c0, sv);
-                    tmem_ld_wait();
-                    float p[16];
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int j = j0 + c0 + u;
-                        const bool vis = valid && j < P.T && __ldg(P.kv_pos + j) <= qp;
-                        p[u] = vis ? exp2f(__uint_as_float(sv[u]) * P.scale_log2 - m_new) : 0.f;
-                    }
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t hi[4], lo[4];
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const float a = p[8 * h + 2 * w], b = p[8 * h + 2 * w + 1];
-                            const __nv_bfloat162 bh = __floats2bfloat162_rn(a, b);
-                            const float2 bf = __bfloat1622float2(bh);
-                            hi[w] = *reinterpret_cast<const uint32_t*>(&bh);
-                            lo[w] = pack_bf16x2(a - bf.x, b - bf.y);
-                        }
-                        const uint32_t off = sw_off(row, c0 / 8 + h);
-                        *reinterpret_cast<uint4*>(sPh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *reinterpret_cast<uint4*>(sPl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    }
-                }
-                m = m_new;
-                // the value tile, transposed into the operand layout: this thread's row is dim `row`
+                // the value tile, transposed into the operand layout while the MMA computes S:
+                // this thread's row is dim `row`
                 if (!wait_all(kv_full, it & 1)) {
                     ok = false;
                     break;
@@ -314,6 +253,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     *reinterpret_cast<uint4*>(sVt + sw_off(row, c)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
+                // the tile's key positions, staged per warp (INT_MAX past the end)
+                int* kpos = wpos + (warp - 2) * TK;
+                {
+                    const int j = j0 + 4 * lane;
+                    int4 p4 = make_int4(INT_MAX, INT_MAX, INT_MAX, INT_MAX);
+                    if (j + 3 < P.T) {
+                        p4 = __ldg(reinterpret_cast<const int4*>(P.kv_pos + j));
+                    } else {
+                        if (j < P.T) p4.x = __ldg(P.kv_pos + j);
+                        if (j + 1 < P.T) p4.y = __ldg(P.kv_pos + j + 1);
+                        if (j + 2 < P.T) p4.z = __ldg(P.kv_pos + j + 2);
+                    }
+                    __syncwarp();  // the warp is done with the previous tile's positions
+                    reinterpret_cast<int4*>(kpos)[lane] = p4;
+                    __syncwarp();
+                }
+                if (!wait_all(s_full, it & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // the whole score row, masked and scaled to base 2
+                uint32_t sv[TK / 16][16];
+#pragma unroll
+                for (int c = 0; c < TK / 16; ++c) tmem_ld16(tl + COL_S + 16 * c, sv[c]);
+                tmem_ld_wait();
+                float mt = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < TK / 16; ++c) {
+#pragma unroll
+                    for (int u = 0; u < 16; u += 4) {
+                        const int4 p4 = reinterpret_cast<const int4*>(kpos)[(16 * c + u) >> 2];
+                        const int pa[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            // positions past the end are INT_MAX; a query at INT_MAX is
+                            // excluded from them by the index test
+                            const bool vis = valid && pa[w] <= qp && j0 + 16 * c + u + w < P.T;
+                            const float v = vis ? __uint_as_float(sv[c][u + w]) * P.scale_log2 : -INFINITY;
+                            sv[c][u + w] = __float_as_uint(v);
+                            mt = fmaxf(mt, v);
+                        }
+                    }
+                }
+                const float m_new = fmaxf(m, mt);
+                const float alpha = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
+                // probabilities as bf16 (hi, lo) in the operand layout
+#pragma unroll
+                for (int c = 0; c < TK / 16; ++c) {
+                    float p[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const float v = __uint_as_float(sv[c][u]);
+                        p[u] = v == -INFINITY ? 0.f : exp2f(v - m_new);
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const float a = p[8 * h + 2 * w], b = p[8 * h + 2 * w + 1];
+                            const __nv_bfloat162 bh = __floats2bfloat162_rn(a, b);
+                            const float2 bf = __bfloat1622float2(bh);
+                            hi[w] = *reinterpret_cast<const uint32_t*>(&bh);
+                            lo[w] = pack_bf16x2(a - bf.x, b - bf.y);
+                        }
+                        const uint32_t off = sw_off(row, 2 * c + h);
+                        *reinterpret_cast<uint4*>(sPh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4*>(sPl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+                m = m_new;
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(p_full);

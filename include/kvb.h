@@ -269,7 +269,9 @@ kvb_status kvb_ridge_solve(kvb_ctx* ctx, kvb_stats* st, const int32_t* sel_k_hos
  * Geometry (L_tgt, H, d) comes from the context's target model; d must be
  * 16, 32, 64 or 128 and n_q_heads a multiple of H.  With T = 0 the cache
  * pointers may be NULL and every cosine is 0; with Tq = 0 nothing is read.
- * fp32 arithmetic throughout.  Asynchronous on `stream`.
+ * KVB_BF16 with d = 128 runs on the tensor cores (exact bf16 products, fp32
+ * accumulation, probabilities carried as a bf16 pair: ~16 significant bits);
+ * everything else in fp32 on CUDA cores.  Asynchronous on `stream`.
  */
 kvb_status kvb_attention_cosine(kvb_ctx* ctx, kvb_dtype dtype, const void* q, int32_t n_q_heads,
                                 const int32_t* q_pos, int64_t Tq, const void* k_a, const void* v_a,

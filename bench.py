@@ -591,7 +591,7 @@ def run_gpu(args, rank, world, local_rank):
     del h_src_k, h_src_v, h_out_k, h_out_v, bufs
 
     # host copy of a bounded sample of the workload for the CPU baseline (rank 0 only)
-    n_l, T_cpu = 4, 4096
+    n_l, T_cpu = 16, 6144  # about 10-15 s of float64 work on the host cores
     sample = None
     if rank == 0:
         tok = torch.arange(0, T_cpu, dtype=torch.int64, device=dev)

@@ -66,6 +66,13 @@ def test_refusals_are_host_side_statuses(lib):
     assert st == 1
     st, _ = _create(lib, _spec(4), _spec(6), max_pos=0)
     assert st == 1
+    # the largest geometry the tables hold: 255 source layers, 128 target layers, k = 16
+    st, _ = _create(lib, _spec(256), _spec(6))
+    assert st == 3 and b"255" in lib.kvb_last_error()
+    st, _ = _create(lib, _spec(40), _spec(129))
+    assert st == 3 and b"128" in lib.kvb_last_error()
+    st, _ = _create(lib, _spec(40), _spec(64), k=17)
+    assert st == 3 and b"16" in lib.kvb_last_error()
 
 
 def test_null_arguments_are_rejected(lib):

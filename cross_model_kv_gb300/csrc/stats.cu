@@ -418,7 +418,7 @@ size_t gather_stream_smem(int d) {
     return static_cast<size_t>(kStages) * kChunk * d * 2   // raw rows
            + static_cast<size_t>(kStages) * d * 4          // running means of the staged slabs
            + static_cast<size_t>(kChunk) * (d / 2) * 8     // RoPE table rows of the chunk
-           + static_cast<size_t>(stream_threads(d) / (d / 2)) * d * 4  // per-row-group column sums
+           + 2 * static_cast<size_t>(stream_threads(d) / (d / 2)) * d * 4  // per-row-group column sums, two slabs
            + 2 * kChunk * 4;                               // row indices, positions
 }
 
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(con
     float* smean = reinterpret_cast<float*>(gsm + static_cast<size_t>(kStages) * kChunk * D * 2);
     float2* stab = reinterpret_cast<float2*>(smean + kStages * D);
     float* red = reinterpret_cast<float*>(stab + kChunk * HALF);
-    int* srow = reinterpret_cast<int*>(red + QN * D);
+    int* srow = reinterpret_cast<int*>(red + 2 * QN * D);
     int* spos = srow + kChunk;
     const int n = *nb;
     const int i = threadIdx.x % HALF;  // RoPE pair (i, i + D/2)
@@ -489,12 +489,26 @@ __global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(con
             if (j < mine) issue(j);
             cp_async_commit();
         }
+        // column sums of slab j-1 (staged in red[(j-1) & 1]) written by the first D threads
+        auto flush_sums = [&](int jj) {
+            const int64_t fp = static_cast<int64_t>(blockIdx.y + jj * gridDim.y) * D;
+            const float* rs = red + (jj & 1) * QN * D;
+            for (int e = threadIdx.x; e < D; e += blockDim.x) {
+                float sm = 0.f;
+#pragma unroll
+                for (int g = 0; g < QN; ++g) sm += rs[g * D + e];
+                part[static_cast<int64_t>(chunk) * F + fp + e] = sm;
+            }
+        };
 #pragma unroll 1
         for (int j = 0; j < mine; ++j) {
+            cp_async_wait<kStages - 2>();
+            // every thread's copies of slab j (and the table) have landed, and every
+            // thread is done with slab j - 1: its stage can be refilled
+            __syncthreads();
+            if (j > 0) flush_sums(j - 1);
             if (j + kStages - 1 < mine) issue(j + kStages - 1);
             cp_async_commit();
-            cp_async_wait<kStages - 1>();
-            __syncthreads();  // every thread's copies of slab j (and the table) have landed
 
             const int slab = blockIdx.y + j * gridDim.y;
             const int64_t f0 = static_cast<int64_t>(slab) * D;
@@ -563,18 +577,12 @@ __global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(con
                 st_global_v8(out + oh + 16 * v, hh);
                 st_global_v8(out_lo + oh + 16 * v, lh);
             }
-            red[q * D + i] = al;
-            red[q * D + HALF + i] = ah;
-            __syncthreads();
-            for (int e = threadIdx.x; e < D; e += blockDim.x) {
-                float sm = 0.f;
-#pragma unroll
-                for (int g = 0; g < QN; ++g) sm += red[g * D + e];
-                part[static_cast<int64_t>(chunk) * F + f0 + e] = sm;
-            }
-            __syncthreads();  // stage j % kStages and the sums are free again
+            red[(j & 1) * QN * D + q * D + i] = al;
+            red[(j & 1) * QN * D + q * D + HALF + i] = ah;
         }
         cp_async_wait<0>();
+        __syncthreads();
+        if (mine > 0) flush_sums(mine - 1);
     }
 }
 

@@ -382,9 +382,9 @@ __global__ void __launch_bounds__(256, (R <= 4 ? 2 : 1)) gather_shift_kernel(con
     }
 }
 
-// Streaming variant of the single-pass gather (head_dim 64 or 128).  A CTA
-// owns one 128-row chunk at a time and walks slabs blockIdx.y, blockIdx.y +
-// gridDim.y, ... of it.  Per chunk the kept-row indices, positions and (for
+// Streaming variant of the single-pass gather (head_dim 64 or 128).  One CTA
+// per SM; the (128-row chunk, slab) work items are split into one contiguous
+// range per CTA, so a CTA walks a run of slabs of one chunk (or two).  Per chunk the kept-row indices, positions and (for
 // keys) the chunk's RoPE table rows are staged in shared memory once; per
 // slab the raw rows are copied in with cp.async, kStages - 1 slabs ahead of
 // the one being processed.  Thread (pair i, row group q) strips pair
@@ -451,8 +451,19 @@ __global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(con
     const int q = threadIdx.x / HALF;  // rows q*ROWS .. q*ROWS + ROWS - 1 of the chunk
     const bool first_batch = *n_seen == 0;
 
+    // work items (chunk, slab) in chunk-major order; CTA b takes one contiguous
+    // range of them, i.e. runs of slabs within one or two chunks
+    const int nchunks = (n + kChunk - 1) / kChunk;
+    const int64_t items = static_cast<int64_t>(nchunks) * n_slabs;
+    const int64_t per = (items + gridDim.x - 1) / gridDim.x;
+    int64_t it0 = blockIdx.x * per;
+    const int64_t it1 = it0 + per < items ? it0 + per : items;
 #pragma unroll 1
-    for (int chunk = blockIdx.x; chunk * kChunk < n; chunk += gridDim.x) {
+    while (it0 < it1) {
+        const int chunk = static_cast<int>(it0 / n_slabs);
+        const int s_begin = static_cast<int>(it0 % n_slabs);
+        const int mine = static_cast<int>(n_slabs - s_begin < it1 - it0 ? n_slabs - s_begin : it1 - it0);
+        it0 += mine;
         const int r0 = chunk * kChunk;
         __syncthreads();  // the previous chunk is done with srow / spos / stab
         for (int t = threadIdx.x; t < kChunk; t += blockDim.x) {
@@ -468,10 +479,8 @@ __global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(con
                 cp_async16(stab + rr * HALF + c2, tab + static_cast<int64_t>(spos[rr]) * HALF + c2, 16);
             }
         }
-        const int mine = (n_slabs - static_cast<int>(blockIdx.y) + static_cast<int>(gridDim.y) - 1) /
-                         static_cast<int>(gridDim.y);
         auto issue = [&](int j) {  // raw rows (and running means) of this CTA's j-th slab into stage j % kStages
-            const int slab = blockIdx.y + j * gridDim.y;
+            const int slab = s_begin + j;
             const __nv_bfloat16* base = cache + static_cast<int64_t>(slab) * T_len * D;
             __nv_bfloat16* dst = stg + static_cast<size_t>(j % kStages) * kChunk * D;
             if (!first_batch && threadIdx.x < D / 4)
@@ -491,7 +500,7 @@ __global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(con
         }
         // column sums of slab j-1 (staged in red[(j-1) & 1]) written by the first D threads
         auto flush_sums = [&](int jj) {
-            const int64_t fp = static_cast<int64_t>(blockIdx.y + jj * gridDim.y) * D;
+            const int64_t fp = static_cast<int64_t>(s_begin + jj) * D;
             const float* rs = red + (jj & 1) * QN * D;
             for (int e = threadIdx.x; e < D; e += blockDim.x) {
                 float sm = 0.f;
@@ -510,7 +519,7 @@ __global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(con
             if (j + kStages - 1 < mine) issue(j + kStages - 1);
             cp_async_commit();
 
-            const int slab = blockIdx.y + j * gridDim.y;
+            const int slab = s_begin + j;
             const int64_t f0 = static_cast<int64_t>(slab) * D;
             const __nv_bfloat16* raw = stg + static_cast<size_t>(j % kStages) * kChunk * D;
             float sl, sh;  // shift of features i and i + D/2
@@ -746,14 +755,7 @@ cudaError_t launch_gather(const GatherArgs& g, cudaStream_t s) {
         const int rps = 256 / (g.d >> 4);
         const int R = rps >= kChunk ? 1 : kChunk / rps;
         if (g.out_lo != nullptr && (g.d == 64 || g.d == 128) && g.num_sms > 0) {
-            const int64_t n_guess = (g.T + g.stride - 1) / g.stride;
-            int64_t gx = (n_guess + kChunk - 1) / kChunk;
-            if (gx > g.num_sms) gx = g.num_sms;
-            if (gx < 1) gx = 1;
-            int64_t gy = g.num_sms / gx;
-            if (gy > g.n_slabs) gy = g.n_slabs;
-            if (gy < 1) gy = 1;
-            dim3 sgrid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+            dim3 sgrid(static_cast<unsigned>(g.num_sms));  // one CTA per SM, work split in-kernel
             const size_t smem = gather_stream_smem(g.d);
             const __nv_bfloat16* c16 = static_cast<const __nv_bfloat16*>(g.cache);
             __nv_bfloat16* o16 = static_cast<__nv_bfloat16*>(g.out);

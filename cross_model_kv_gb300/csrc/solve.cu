@@ -330,19 +330,28 @@ cudaError_t update(const TcSolve* tc, const float* A, int64_t a_row, int64_t a_k
 
 }  // namespace
 
-// Right-looking blocked Cholesky with 128-wide super-panels: the two 64-wide
-// halves are factored one after the other (the second half's columns updated
-// by the first half's panel alone), then the trailing matrix takes one
-// rank-128 update, which halves its read-modify-write passes against 64-wide
-// steps.
+// Right-looking blocked Cholesky with super-panels of NSUB 64-wide steps: each
+// step's columns are first brought up to date with the earlier steps of the
+// same super-panel (left-looking inside it), factored and inverted on the
+// diagonal and multiplied into the panel below; the trailing matrix then takes
+// one rank-(NSUB * 64) update, so it is read and written once per super-panel.
+constexpr int NSUB = 4;
+constexpr int SP = NSUB * NB;
+
 cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t n, int batch, int* numeric_flag,
                                 float* Linv, int64_t strideL, const TcSolve* tc, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
-    for (int64_t k0 = 0; k0 < n; k0 += 2 * NB) {
-        for (int half = 0; half < 2; ++half) {
-            const int64_t j0 = k0 + half * NB;  // first column of this 64-wide half
+    for (int64_t k0 = 0; k0 < n; k0 += SP) {
+        for (int i = 0; i < NSUB; ++i) {
+            const int64_t j0 = k0 + static_cast<int64_t>(i) * NB;  // first column of this step
             if (j0 >= n) break;
             const int nb = static_cast<int>(n - j0 < NB ? n - j0 : NB);
+            if (i > 0) {  // columns j0.. of rows j0.. minus the earlier steps of this super-panel
+                const float* Pp = G + j0 * ldg + k0;  // (n - j0) x (j0 - k0)
+                e = update(tc, Pp, ldg, 1, strideG, n - j0, Pp, ldg, 1, strideG, nb, static_cast<int>(j0 - k0),
+                           G + j0 * ldg + j0, ldg, strideG, -1.f, 1.f, false, batch, s);
+                if (e != cudaSuccess) return e;
+            }
             potrf_diag_kernel<<<batch, 256, 0, s>>>(G, ldg, strideG, j0, nb, numeric_flag, Linv, strideL);
             const int64_t rem = n - j0 - nb;
             if (rem <= 0) break;
@@ -351,19 +360,12 @@ cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t 
             e = update(nullptr, G + (j0 + nb) * ldg + j0, ldg, 1, strideG, rem, Linv + j0 * NB, NB, 1, strideL, nb,
                        nb, G + (j0 + nb) * ldg + j0, ldg, strideG, 1.f, 0.f, false, batch, s);
             if (e != cudaSuccess) return e;
-            if (half == 0 && rem > 0) {  // the second half's columns, rows below the first half
-                const int nb2 = static_cast<int>(rem < NB ? rem : NB);
-                const float* P1 = G + (j0 + nb) * ldg + j0;
-                e = update(nullptr, P1, ldg, 1, strideG, rem, P1, ldg, 1, strideG, nb2, nb,
-                           G + (j0 + nb) * ldg + (j0 + nb), ldg, strideG, -1.f, 1.f, false, batch, s);
-                if (e != cudaSuccess) return e;
-            }
         }
-        const int64_t t0 = k0 + 2 * NB;  // trailing matrix of the super-panel
+        const int64_t t0 = k0 + SP;  // trailing matrix of the super-panel
         if (t0 >= n) break;
-        const float* P = G + t0 * ldg + k0;  // (n - t0) x 128
-        e = update(tc, P, ldg, 1, strideG, n - t0, P, ldg, 1, strideG, n - t0, 2 * NB, G + t0 * ldg + t0, ldg,
-                   strideG, -1.f, 1.f, true, batch, s);
+        const float* P = G + t0 * ldg + k0;  // (n - t0) x SP
+        e = update(tc, P, ldg, 1, strideG, n - t0, P, ldg, 1, strideG, n - t0, SP, G + t0 * ldg + t0, ldg, strideG,
+                   -1.f, 1.f, true, batch, s);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
@@ -395,43 +397,46 @@ cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int
         return launch_gemm_f32(t, s);
     };
     cudaError_t e;
-    // forward, L Y = C, 128 rows at a time: Y1 = L11^-1 C1; C2 -= L21 Y1; Y2 = L22^-1 C2;
-    // then one rank-128 update of every row below
-    for (int64_t k0 = 0; k0 < n; k0 += 2 * NB) {
-        const int nb1 = static_cast<int>(n - k0 < NB ? n - k0 : NB);
-        const int nb2 = static_cast<int>(n - k0 - nb1 <= 0 ? 0 : (n - k0 - nb1 < NB ? n - k0 - nb1 : NB));
-        if ((e = diag(k0, nb1, false)) != cudaSuccess) return e;
-        if (nb2 > 0) {
-            // B(k, n) = C[k0 + k][n]: row stride 1, k stride ldc
-            e = update(nullptr, L + (k0 + NB) * ldg + k0, ldg, 1, strideG, nb2, C + k0 * ldc, 1, ldc, strideC, m,
-                       nb1, C + (k0 + NB) * ldc, ldc, strideC, -1.f, 1.f, false, batch, s);
-            if (e != cudaSuccess) return e;
-            if ((e = diag(k0 + NB, nb2, false)) != cudaSuccess) return e;
+    // forward, L Y = C, one super-block of rows at a time: each 64-row step takes
+    // the earlier steps of its super-block, then its inverse diagonal block; then
+    // one rank-(NSUB * 64) update of every row below.  B(k, n) = C[k][n]: row
+    // stride 1, k stride ldc.
+    for (int64_t k0 = 0; k0 < n; k0 += SP) {
+        const int64_t kend = k0 + SP < n ? k0 + SP : n;
+        for (int64_t j0 = k0; j0 < kend; j0 += NB) {
+            const int nb = static_cast<int>(kend - j0 < NB ? kend - j0 : NB);
+            if (j0 > k0) {
+                e = update(tc, L + j0 * ldg + k0, ldg, 1, strideG, nb, C + k0 * ldc, 1, ldc, strideC, m,
+                           static_cast<int>(j0 - k0), C + j0 * ldc, ldc, strideC, -1.f, 1.f, false, batch, s);
+                if (e != cudaSuccess) return e;
+            }
+            if ((e = diag(j0, nb, false)) != cudaSuccess) return e;
         }
-        const int64_t t0 = k0 + nb1 + nb2;
-        if (t0 >= n) break;
-        e = update(tc, L + t0 * ldg + k0, ldg, 1, strideG, n - t0, C + k0 * ldc, 1, ldc, strideC, m, nb1 + nb2,
-                   C + t0 * ldc, ldc, strideC, -1.f, 1.f, false, batch, s);
+        if (kend >= n) break;
+        e = update(tc, L + kend * ldg + k0, ldg, 1, strideG, n - kend, C + k0 * ldc, 1, ldc, strideC, m,
+                   static_cast<int>(kend - k0), C + kend * ldc, ldc, strideC, -1.f, 1.f, false, batch, s);
         if (e != cudaSuccess) return e;
     }
-    // backward, L^T X = Y, last super-block first: X2 = L22^-T Y2; Y1 -= L21^T X2;
-    // X1 = L11^-T Y1; then one rank-128 update of every row above
-    const int64_t last = ((n - 1) / (2 * NB)) * (2 * NB);
-    for (int64_t k0 = last; k0 >= 0; k0 -= 2 * NB) {
-        const int nb1 = static_cast<int>(n - k0 < NB ? n - k0 : NB);
-        const int nb2 = static_cast<int>(n - k0 - nb1 <= 0 ? 0 : (n - k0 - nb1 < NB ? n - k0 - nb1 : NB));
-        if (nb2 > 0) {
-            if ((e = diag(k0 + NB, nb2, true)) != cudaSuccess) return e;
-            // A(i, kk) = L[k0 + NB + kk][k0 + i]: row stride 1, k stride ldg
-            e = update(nullptr, L + (k0 + NB) * ldg + k0, 1, ldg, strideG, nb1, C + (k0 + NB) * ldc, 1, ldc, strideC,
-                       m, nb2, C + k0 * ldc, ldc, strideC, -1.f, 1.f, false, batch, s);
-            if (e != cudaSuccess) return e;
+    // backward, L^T X = Y, last super-block first; inside it the last step first,
+    // each step taking the later steps of the super-block; then one rank-(NSUB * 64)
+    // update of every row above.  A(i, kk) = L[row0 + kk][col0 + i]: row stride 1,
+    // k stride ldg.
+    const int64_t last = ((n - 1) / SP) * SP;
+    for (int64_t k0 = last; k0 >= 0; k0 -= SP) {
+        const int64_t kend = k0 + SP < n ? k0 + SP : n;
+        for (int64_t j0 = k0 + ((kend - 1 - k0) / NB) * NB; j0 >= k0; j0 -= NB) {
+            const int nb = static_cast<int>(kend - j0 < NB ? kend - j0 : NB);
+            if (j0 + nb < kend) {
+                e = update(tc, L + (j0 + nb) * ldg + j0, 1, ldg, strideG, nb, C + (j0 + nb) * ldc, 1, ldc, strideC,
+                           m, static_cast<int>(kend - j0 - nb), C + j0 * ldc, ldc, strideC, -1.f, 1.f, false, batch,
+                           s);
+                if (e != cudaSuccess) return e;
+            }
+            if ((e = diag(j0, nb, true)) != cudaSuccess) return e;
         }
-        if ((e = diag(k0, nb1, true)) != cudaSuccess) return e;
         if (k0 == 0) break;
-        // rows above: A(i, kk) = L[k0 + kk][i] for i < k0
-        e = update(tc, L + k0 * ldg, 1, ldg, strideG, k0, C + k0 * ldc, 1, ldc, strideC, m, nb1 + nb2, C, ldc,
-                   strideC, -1.f, 1.f, false, batch, s);
+        e = update(tc, L + k0 * ldg, 1, ldg, strideG, k0, C + k0 * ldc, 1, ldc, strideC, m,
+                   static_cast<int>(kend - k0), C, ldc, strideC, -1.f, 1.f, false, batch, s);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

@@ -3,8 +3,8 @@
 //
 // The ridge systems of the fit ("KVBridge" README, "Loading": W = (M +
 // lambda I)^-1 C) and of the single-source R^2 ("What ships") are solved in
-// float32 by a blocked Cholesky whose work is rank-128 (and rank-64) updates
-//     C = alpha * A B^T + beta * C      (A: M x K, B: N x K, K <= 128, C fp32)
+// float32 by a blocked Cholesky whose work is rank-256 (and smaller) updates
+//     C = alpha * A B^T + beta * C      (A: M x K, B: N x K, K <= 256, C fp32)
 // of the trailing matrix and of the right-hand sides.  Here every fp32
 // operand x is carried as three bf16 parts, x1 = bf16(x), x2 = bf16(x - x1),
 // x3 = bf16(x - x1 - x2) (24 significant bits in all), and the product is
@@ -32,7 +32,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;  // one 128-byte swizzle atom of bf16
-constexpr int KMAX = 128;  // largest update rank
+constexpr int KMAX = 256;  // largest update rank
 constexpr int STAGES = 2;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
@@ -49,7 +49,7 @@ __constant__ int kPartB[NPROD] = {0, 1, 0, 2, 1, 0};
 struct Params {
     float* C;
     int64_t ldc, strideC;
-    int M, N, lower, nkb;  // nkb: 64-wide K blocks (1 or 2)
+    int M, N, lower, nkb;  // nkb: 64-wide K blocks (1 to 4)
     float alpha, beta;
     DevErr err;
 };
@@ -296,7 +296,9 @@ size_t tc_update_ws_bytes(int64_t rows_a, int64_t rows_b, int batch) {
 }
 
 bool tc_update_supported(const TcSolve* tc, int64_t M, int64_t N, int K, const float* C, int64_t ldc) {
-    return tc && tc->ws && tc->num_sms > 0 && K >= 1 && K <= KMAX && M >= 256 && N >= 256 && N % 16 == 0 && ldc % 4 == 0 &&
+    // worth a launch when the update is large: many rows, or a few rows across many columns
+    const bool large = (M >= 256 && N >= 256) || (M >= 64 && N >= 8192);
+    return tc && tc->ws && tc->num_sms > 0 && K >= 1 && K <= KMAX && large && N % 16 == 0 && ldc % 4 == 0 &&
            (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && M <= 0x7fffffffLL && N <= 0x7fffffffLL;
 }
 
@@ -308,7 +310,7 @@ cudaError_t launch_tc_update(const TcSolve& tc, const TcOperand& A, const TcOper
         if (why) *why = "tensor-core update workspace too small";
         return cudaErrorInvalidValue;
     }
-    const int kp = K <= BK ? BK : KMAX;
+    const int kp = ((K + BK - 1) / BK) * BK;
     __nv_bfloat16* wa = tc.ws;
     __nv_bfloat16* wb = wa + 3 * static_cast<int64_t>(batch) * A.rows * kp;
     cudaError_t e = split3(A, K, kp, batch, wa, s);

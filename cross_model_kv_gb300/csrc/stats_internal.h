@@ -101,13 +101,13 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm_f32(const GemmArgs& g, cudaStream_t s);
 
-// In-place blocked Cholesky of batch SPD matrices (lower triangle used; 128-wide
-// super-panels of two 64-wide steps), then in-place solve of G X = C for m
+// In-place blocked Cholesky of batch SPD matrices (lower triangle used; 256-wide
+// super-panels of four 64-wide steps), then in-place solve of G X = C for m
 // right-hand sides.  The factor also leaves the inverse of every 64 x 64 diagonal block in Linv
 // ([batch][n/64 * 64][64], strideL floats per system), so both triangular
 // solves run as GEMMs.  A non-positive pivot sets *numeric_flag.
-// Rank <= 128 updates on the tensor cores with fp32 operands carried as three
-// bf16 parts (solve_tc_sm103.cu).  An operand is rows x K (K <= 128) fp32 with
+// Rank <= 256 updates on the tensor cores with fp32 operands carried as three
+// bf16 parts (solve_tc_sm103.cu).  An operand is rows x K (K <= 256) fp32 with
 // element (r, k) of batch item b at src[b * s_batch + r * s_row + k * s_k].
 struct TcOperand {
     const float* src;
@@ -126,7 +126,7 @@ cudaError_t launch_tc_update(const TcSolve& tc, const TcOperand& A, const TcOper
                              int64_t strideC, float alpha, float beta, bool lower, int batch, cudaStream_t s,
                              std::string* why);
 
-// tc (may be NULL): run the large rank-128 updates on the tensor cores.
+// tc (may be NULL): run the large updates on the tensor cores.
 cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t n, int batch, int* numeric_flag,
                                 float* Linv, int64_t strideL, const TcSolve* tc, cudaStream_t s);
 cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int64_t n, const float* Linv,

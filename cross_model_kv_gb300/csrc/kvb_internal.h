@@ -56,6 +56,11 @@ struct MapGemmArgs {
     const void* a_lo[2];    // lo parts when split
     const void* w_lo[2];
     bool split;
+    // strip fused into the kernel: a_src[0] is then written by the kernel from k_raw
+    bool fuse_strip;
+    const void* k_raw;      // [L_s*H][T][d] bf16 source keys as stored
+    const float2* tab_s;    // source RoPE table
+    int* strip_ctr;         // [2] zeroed before the launch
     const float* bias[2];   // [L_t][q]
     void* out[2];           // [L_t][H][T][d] bf16 (fp32 when split)
     const int* pos;
@@ -65,6 +70,7 @@ struct MapGemmArgs {
     int num_sms;
 };
 bool map_gemm_tc_supported(const Shape& sh);
+bool map_gemm_fused_strip_supported(const Shape& sh);
 cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string* why);
 
 // SIMT mapper (any even d with d % 8 == 0): strip fused into the operand load,

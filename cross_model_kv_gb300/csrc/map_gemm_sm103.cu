@@ -71,6 +71,15 @@ struct Params {
     const float2* tab_t;
     DevErr err;
     SelTable sel;
+    // strip fused into the kernel (bf16 single-CTA kernel): value tiles run
+    // first while the epilogue warps strip the source keys chunk by chunk
+    int fuse_strip;
+    const __nv_bfloat16* k_raw;  // [L_s*H][T][d] source keys as stored
+    __nv_bfloat16* k_strip;      // same layout, stripped: the key tiles' A operand
+    const float2* tab_s;
+    int* strip_ctr;              // [0] next chunk to claim, [1] chunks finished
+    int strip_chunks;            // chunks of 128 tokens per (layer, head) slab
+    int strip_items;             // all chunks
 };
 
 struct TileCoord {
@@ -85,7 +94,49 @@ __device__ __forceinline__ TileCoord decode_tile(const Params& P, int tile) {
     r /= P.num_m;
     c.t = r % P.L_t;
     c.kv = r / P.L_t;
+    if (P.fuse_strip) c.kv = 1 - c.kv;  // value tiles first: their operand needs no strip
     return c;
+}
+
+// One warp strips 128 tokens of one (layer, head) slab of the source keys:
+// eight lanes per row, each owning 8 RoPE pairs (two 16-byte loads and stores,
+// the (cos, sin) of its pairs from the table), rotation by -angle.  A position
+// outside the table is recorded and its row written as zeros.
+__device__ __forceinline__ void strip_chunk(const Params& P, int item, int lane) {
+    const int slab = item / P.strip_chunks;
+    const int t0 = (item - slab * P.strip_chunks) * 128;
+    const int half = P.d >> 1;
+    const int c8 = (lane & 7) * 8;  // first pair of this lane
+#pragma unroll 2
+    for (int r = lane >> 3; r < 128; r += 4) {
+        const int tok = t0 + r;
+        if (tok >= P.T) break;
+        const int64_t o = (static_cast<int64_t>(slab) * P.T + tok) * P.d + c8;
+        const int p = __ldg(P.pos + tok);
+        uint4 olo = make_uint4(0, 0, 0, 0), ohi = make_uint4(0, 0, 0, 0);
+        if (p < 0 || p >= P.max_pos) {
+            dev_err_set(P.err, DEV_ERR_BAD_POS);
+        } else {
+            const uint4 vlo = __ldcs(reinterpret_cast<const uint4*>(P.k_raw + o));
+            const uint4 vhi = __ldcs(reinterpret_cast<const uint4*>(P.k_raw + o + half));
+            const float4* tp = reinterpret_cast<const float4*>(P.tab_s + static_cast<int64_t>(p) * half + c8);
+            const __nv_bfloat162* lo2 = reinterpret_cast<const __nv_bfloat162*>(&vlo);
+            const __nv_bfloat162* hi2 = reinterpret_cast<const __nv_bfloat162*>(&vhi);
+            uint32_t wl[4], wh[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 cs = __ldg(tp + q);  // (c, s) of pairs 2q and 2q+1
+                const float2 l = __bfloat1622float2(lo2[q]);
+                const float2 h = __bfloat1622float2(hi2[q]);
+                wl[q] = pack_bf16x2(fmaf(l.x, cs.x, h.x * cs.y), fmaf(l.y, cs.z, h.y * cs.w));
+                wh[q] = pack_bf16x2(fmaf(h.x, cs.x, -(l.x * cs.y)), fmaf(h.y, cs.z, -(l.y * cs.w)));
+            }
+            olo = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            ohi = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        }
+        *reinterpret_cast<uint4*>(P.k_strip + o) = olo;
+        *reinterpret_cast<uint4*>(P.k_strip + o + half) = ohi;
+    }
 }
 
 // K-block kb of target layer t: (source layer, head, first dim) of its box.
@@ -254,8 +305,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int issued_phase[STAGES];
             for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
             bool ok = true;
+            bool stripped = !P.fuse_strip;
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
                 const TileCoord c = decode_tile(P, tile);
+                if (c.kv == 0 && !stripped) {
+                    // every chunk of the stripped keys is written (by any CTA) before
+                    // the first key tile is loaded; bounded like every other wait
+                    const uint64_t t0 = global_timer_ns();
+                    while (ld_acquire_gpu(P.strip_ctr + 1) < P.strip_items) {
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        if (global_timer_ns() - t0 > P.err.timeout_ns) {
+                            dev_err_set(P.err, DEV_ERR_TIMEOUT);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(256);
+                    }
+                    if (!ok) break;
+                    fence_proxy_async_global();  // the TMA loads below see the generic-proxy writes
+                    stripped = true;
+                }
                 for (int ki = 0; ki < nk_issue; ++ki) {
                     const int kb = SPLIT ? ki / 3 : ki;
                     const int seg = SPLIT ? ki - 3 * kb : 0;  // 0: hi x hi, 1: hi x lo, 2: lo x hi
@@ -328,8 +401,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = sub * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
+        bool strip_left = P.fuse_strip != 0;  // warp-uniform
         for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
             const TileCoord c = decode_tile(P, tile);
+            // while the accumulator is not ready, strip chunks of the source keys
+            while (strip_left && !__any_sync(0xffffffffu, mbar_try_wait(&tfull[acc], acc_phase))) {
+                int item = 0;
+                if (lane == 0) item = *abort_flag ? P.strip_items : atomicAdd(P.strip_ctr, 1);
+                item = __shfl_sync(0xffffffffu, item, 0);
+                if (item >= P.strip_items) {
+                    strip_left = false;
+                    break;
+                }
+                strip_chunk(P, item, lane);
+                fence_proxy_async_global();  // for the TMA loads of other CTAs
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();  // the warp's stores before the count (release)
+                    atomicAdd(P.strip_ctr + 1, 1);
+                }
+            }
             if (!mbar_wait(&tfull[acc], acc_phase, P.err, abort_flag)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
@@ -549,6 +640,11 @@ bool map_gemm_tc_supported(const Shape& sh) {
     return sh.d == 128 && q % BN == 0 && sh.L_t <= MAX_LT && sh.T <= 0x7fffffffLL;
 }
 
+bool map_gemm_fused_strip_supported(const Shape& sh) {
+    return map_gemm_tc_supported(sh) && !use_pair_kernel() &&
+           static_cast<int64_t>(sh.L_s) * sh.H * ((sh.T + 127) / 128) < 0x7fffffffLL;
+}
+
 cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string* why) {
     const Shape& sh = a.sh;
     const int q = sh.H * sh.d;
@@ -574,6 +670,15 @@ cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string
     P.tab_t = a.tab_t;
     P.err = a.err;
     P.sel = a.sel;
+    if (a.fuse_strip && !a.split) {
+        P.fuse_strip = 1;
+        P.k_raw = static_cast<const __nv_bfloat16*>(a.k_raw);
+        P.k_strip = static_cast<__nv_bfloat16*>(const_cast<void*>(a.a_src[0]));
+        P.tab_s = a.tab_s;
+        P.strip_ctr = a.strip_ctr;
+        P.strip_chunks = static_cast<int>((sh.T + 127) / 128);
+        P.strip_items = static_cast<int>(static_cast<int64_t>(sh.L_s) * sh.H * P.strip_chunks);
+    }
     for (int kv = 0; kv < 2; ++kv) {
         P.bias[kv] = a.bias[kv];
         P.out[kv] = a.out[kv];

@@ -114,6 +114,29 @@ def test_fp32_bad_position_is_reported_and_row_zeroed(kvb):
     kvb.kvb_ctx_check(ctx)
 
 
+def test_fused_and_separate_strip_give_identical_bits(kvb, monkeypatch):
+    # the strip runs inside the map kernel by default (epilogue warps, during the
+    # value tiles); KVB_MAP_FUSED_STRIP=0 runs the separate strip pass instead
+    pos = np.random.default_rng(6).integers(0, 30000, size=1500).astype(np.int32)
+    c = ApplyCase(6, 4, 4, 128, 3, 1500, 1e4, 1e6, torch.bfloat16, seed=38, positions=pos)
+    ctx = _ctx(kvb, c, 30000)
+    kvb.kvb_profile_enable(ctx, True)
+    c.run(kvb, ctx)
+    kvb.kvb_ctx_check(ctx)
+    assert "rope_strip_bf16" not in kvb.kvb_profile_read(ctx)
+    fused = (c.out_k.clone(), c.out_v.clone())
+    monkeypatch.setenv("KVB_MAP_FUSED_STRIP", "0")
+    c.out_k.zero_()
+    c.out_v.zero_()
+    c.run(kvb, ctx)
+    kvb.kvb_ctx_check(ctx)
+    assert "rope_strip_bf16" in kvb.kvb_profile_read(ctx)
+    assert torch.equal(fused[0], c.out_k) and torch.equal(fused[1], c.out_v)
+    ok, ov = c.oracle([0, 3], None)
+    gk, gv = c.gpu([0, 3], None)
+    assert rel_fro(gk, ok) <= TOL_BF16 and rel_fro(gv, ov) <= TOL_BF16
+
+
 def test_empty_input_is_a_no_op(kvb):
     c = ApplyCase(2, 2, 2, 128, 1, 0, 1e4, 1e4, torch.bfloat16, seed=26)
     ctx = _ctx(kvb, c, 8)

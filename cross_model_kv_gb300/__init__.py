@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     kvb_stats_accumulate,
     kvb_stats_count,
     kvb_stats_create,
+    kvb_stats_create_block,
     kvb_stats_destroy,
     kvb_stats_export,
     kvb_stats_import,

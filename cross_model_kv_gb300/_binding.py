@@ -62,6 +62,8 @@ SIGNATURES = {
     "kvb_map_apply_noalloc": (ctypes.c_int, [_SPEC_P, _SPEC_P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P,
                                              ctypes.c_int64, _I32P, _I32P, _P, _P, _P, _P, _P, _P, _P]),
     "kvb_stats_create": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.POINTER(_P)]),
+    "kvb_stats_create_block": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.POINTER(_P)]),
     "kvb_stats_destroy": (ctypes.c_int, [_P]),
     "kvb_stats_reset": (ctypes.c_int, [_P, _P]),
     "kvb_stats_accumulate": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int32, _P]),
@@ -256,6 +258,14 @@ def kvb_stats_create(ctx: Ctx, dtype: int, max_batch_tokens: int) -> Stats:
     return Stats(h, ctx, int(dtype))
 
 
+def kvb_stats_create_block(ctx: Ctx, dtype: int, max_batch_tokens: int, t_begin: int, t_end: int) -> Stats:
+    """Statistics of target layers [t_begin, t_end) only (bounded memory; one calibration pass per block)."""
+    h = ctypes.c_void_p()
+    _check(load_library().kvb_stats_create_block(ctx.handle, int(dtype), int(max_batch_tokens), int(t_begin),
+                                                 int(t_end), ctypes.byref(h)))
+    return Stats(h, ctx, int(dtype))
+
+
 def kvb_stats_destroy(st: Stats):
     if st.handle:
         _check(load_library().kvb_stats_destroy(st.handle))
@@ -293,10 +303,17 @@ def kvb_stats_import(st: Stats, kv: int, n_obs: int, mean_x, mean_y, gram, cross
                                            _dev(cross), _dev(syy), _stream(stream)))
 
 
-def kvb_layer_select(ctx: Ctx, st: Stats, lam: float = 0.01, r2=None, stream=None):
-    """Returns (sel_k, sel_v) as int32 numpy arrays [L_t][k]; fills r2 [2][L_t][L_s] if given."""
-    sk = np.zeros((ctx.L_t, ctx.k), dtype=np.int32)
-    sv = np.zeros((ctx.L_t, ctx.k), dtype=np.int32)
+def kvb_layer_select(ctx: Ctx, st: Stats, lam: float = 0.01, r2=None, stream=None, sel_k=None, sel_v=None):
+    """Returns (sel_k, sel_v) as int32 numpy arrays [L_t][k]; fills r2 [2][L_t][L_s] if given.
+
+    With block statistics only the block's rows are written: pass the arrays of
+    earlier blocks as sel_k / sel_v (int32, [L_t][k], C-contiguous) to fill them in place.
+    """
+    sk = np.zeros((ctx.L_t, ctx.k), dtype=np.int32) if sel_k is None else sel_k
+    sv = np.zeros((ctx.L_t, ctx.k), dtype=np.int32) if sel_v is None else sel_v
+    for a in (sk, sv):
+        if a.dtype != np.int32 or a.shape != (ctx.L_t, ctx.k) or not a.flags.c_contiguous:
+            raise ValueError(f"selection arrays must be C-contiguous int32 [{ctx.L_t}][{ctx.k}]")
     _check(load_library().kvb_layer_select(ctx.handle, st.handle, float(lam), sk.ctypes.data_as(_I32P),
                                            sv.ctypes.data_as(_I32P), _dev(r2), _stream(stream)))
     return sk, sv

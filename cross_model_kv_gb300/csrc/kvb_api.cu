@@ -48,9 +48,11 @@ kvb_status check_device_ptrs(std::initializer_list<const void*> ptrs, const char
     return KVB_OK;
 }
 
-kvb_status check_selection(const kvb_ctx* c, const int32_t* sel, const char* name, SelTable* tab, int kv) {
+kvb_status check_selection(const kvb_ctx* c, const int32_t* sel, const char* name, SelTable* tab, int kv,
+                           int t_begin, int t_end) {
     if (!sel) return fail(KVB_ERR_INVALID_ARG, std::string(name) + " is NULL");
-    for (int t = 0; t < c->L_t; ++t) {
+    if (t_end < 0) t_end = c->L_t;
+    for (int t = t_begin; t < t_end; ++t) {
         for (int j = 0; j < c->k; ++j) {
             const int32_t v = sel[t * c->k + j];
             if (v < 0 || v >= c->L_s)

@@ -39,7 +39,9 @@ kvb_status fail(kvb_status s, const std::string& msg);
 kvb_status cuda_fail(cudaError_t e, const char* what);
 bool aligned16(const void* p);
 kvb_status check_device_ptrs(std::initializer_list<const void*> ptrs, const char* what);
-kvb_status check_selection(const kvb_ctx* c, const int32_t* sel, const char* name, SelTable* tab, int kv);
+// Rows [t_begin, t_end) of a [L_tgt][k] selection (t_end < 0: all rows).
+kvb_status check_selection(const kvb_ctx* c, const int32_t* sel, const char* name, SelTable* tab, int kv,
+                           int t_begin = 0, int t_end = -1);
 kvb_status take_device_error(kvb_ctx* c);
 void mirror_device_error(kvb_ctx* c, cudaStream_t s);
 DevErr dev_err(const kvb_ctx* c);

@@ -18,7 +18,8 @@ struct kvb_stats {
     kvb_ctx* ctx = nullptr;
     kvb_dtype dtype = KVB_BF16;
     int64_t max_T = 0, ld = 0;  // ld: columns of the compact batch matrices (multiple of 64)
-    int64_t Fs = 0, Ft = 0;     // all source features, all target columns
+    int64_t Fs = 0, Ft = 0;     // all source features; target columns of the block
+    int t0 = 0, nt = 0;         // target layers [t0, t0 + nt) held by this object
     long long* n_dev = nullptr;
     int* nb_dev = nullptr;
     float* coef_dev = nullptr;  // {f = n_a n_b / n, g = n_b} of the current batch
@@ -159,8 +160,20 @@ extern "C" {
 
 kvb_status kvb_stats_create(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_batch_tokens, kvb_stats** out) {
     g_last_error.clear();
+    if (!ctx) {
+        if (out) *out = nullptr;
+        return fail(KVB_ERR_INVALID_ARG, "NULL argument");
+    }
+    return kvb_stats_create_block(ctx, dtype, max_batch_tokens, 0, ctx->L_t, out);
+}
+
+kvb_status kvb_stats_create_block(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_batch_tokens, int32_t t_begin,
+                                  int32_t t_end, kvb_stats** out) {
+    g_last_error.clear();
     if (out) *out = nullptr;
     if (!ctx || !out) return fail(KVB_ERR_INVALID_ARG, "NULL argument");
+    if (t_begin < 0 || t_end <= t_begin || t_end > ctx->L_t)
+        return fail(KVB_ERR_INVALID_ARG, "target block must satisfy 0 <= t_begin < t_end <= L_tgt");
     if (dtype != KVB_F32 && dtype != KVB_BF16) return fail(KVB_ERR_UNSUPPORTED, "dtype must be KVB_F32 or KVB_BF16");
     if (max_batch_tokens < 1 || max_batch_tokens > (int64_t(1) << 30))
         return fail(KVB_ERR_INVALID_ARG, "max_batch_tokens must be in [1, 2^30]");
@@ -173,7 +186,9 @@ kvb_status kvb_stats_create(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_batch_tok
     st->ld = (max_batch_tokens + 127) & ~int64_t(127);  // whole 128-row gather chunks
     const int64_t q = static_cast<int64_t>(ctx->H) * ctx->d;
     st->Fs = ctx->L_s * q;
-    st->Ft = ctx->L_t * q;
+    st->t0 = t_begin;
+    st->nt = t_end - t_begin;
+    st->Ft = st->nt * q;
     kvb_status s = KVB_OK;
     auto A = [&](void** p, size_t bytes) {
         if (s == KVB_OK) s = st_alloc(st, p, bytes);
@@ -269,8 +284,11 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const DevErr err = dev_err(c);
     const kvb_dtype dt = st->dtype;
-    const int64_t LsH = static_cast<int64_t>(c->L_s) * c->H, LtH = static_cast<int64_t>(c->L_t) * c->H;
-    const void* caches[4] = {src_k, src_v, tgt_k, tgt_v};
+    const int64_t LsH = static_cast<int64_t>(c->L_s) * c->H, LtH = static_cast<int64_t>(st->nt) * c->H;
+    // the block's target layers: [t0, t0 + nt) of the [L_tgt][H][T][d] target caches
+    const size_t tgt_off = static_cast<size_t>(st->t0) * c->H * static_cast<size_t>(T) * c->d * (dt == KVB_F32 ? 4 : 2);
+    const void* caches[4] = {src_k, src_v, static_cast<const char*>(tgt_k) + tgt_off,
+                             static_cast<const char*>(tgt_v) + tgt_off};
     const int64_t slabs[4] = {LsH, LsH, LtH, LtH};
     const float2* tabs[4] = {c->tab_s, nullptr, c->tab_t, nullptr};
     void* outs[4] = {st->XT[0], st->XT[1], st->YT[0], st->YT[1]};
@@ -451,15 +469,20 @@ kvb_status kvb_layer_select(kvb_ctx* c, kvb_stats* st, double lambda, int32_t* s
                     e = launch_sse(st->cross[kv], Ft, L, q, q, Ft, st->wsD, st->wsR, int64_t(q) * Ft, st->syy[kv], lam,
                                    st->wsS, nb, cs);
                 if (e == cudaSuccess)
-                    e = launch_r2_head(st->wsS, Ft, st->syy[kv], c->L_t, c->H, c->d, L,
-                                       st->r2 + size_t(kv) * c->L_t * c->L_s, c->L_s, nb, cs);
+                    e = launch_r2_head(st->wsS, Ft, st->syy[kv], st->nt, c->H, c->d, L,
+                                       st->r2 + (size_t(kv) * c->L_t + st->t0) * c->L_s, c->L_s, nb, cs);
             }
         }
-        if (e == cudaSuccess) e = launch_topk(st->r2, 2 * c->L_t, c->L_s, c->k, st->sel, cs);
+        for (int kv = 0; kv < 2 && e == cudaSuccess; ++kv)
+            e = launch_topk(st->r2 + (size_t(kv) * c->L_t + st->t0) * c->L_s, st->nt, c->L_s, c->k,
+                            st->sel + (size_t(kv) * c->L_t + st->t0) * c->k, cs);
     }
     if (e != cudaSuccess) return cuda_fail(e, "layer selection");
-    if (r2_out) {
-        e = cudaMemcpyAsync(r2_out, st->r2, 2ull * c->L_t * c->L_s * 4, cudaMemcpyDeviceToDevice, cs);
+    if (r2_out) {  // the block's rows only
+        for (int kv = 0; kv < 2 && e == cudaSuccess; ++kv) {
+            const size_t off = (size_t(kv) * c->L_t + st->t0) * c->L_s;
+            e = cudaMemcpyAsync(r2_out + off, st->r2 + off, size_t(st->nt) * c->L_s * 4, cudaMemcpyDeviceToDevice, cs);
+        }
         if (e != cudaSuccess) return cuda_fail(e, "copying R^2");
     }
     std::vector<int32_t> sel(2ull * c->L_t * c->k);
@@ -468,8 +491,9 @@ kvb_status kvb_layer_select(kvb_ctx* c, kvb_stats* st, double lambda, int32_t* s
     if (e == cudaSuccess) e = cudaMemcpyAsync(&numeric, st->numeric, sizeof(int), cudaMemcpyDeviceToHost, cs);
     if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
     if (e != cudaSuccess) return cuda_fail(e, "layer selection");
-    std::memcpy(sel_k_host, sel.data(), size_t(c->L_t) * c->k * 4);
-    std::memcpy(sel_v_host, sel.data() + size_t(c->L_t) * c->k, size_t(c->L_t) * c->k * 4);
+    const size_t o = size_t(st->t0) * c->k, n_sel = size_t(st->nt) * c->k;
+    std::memcpy(sel_k_host + o, sel.data() + o, n_sel * 4);
+    std::memcpy(sel_v_host + o, sel.data() + size_t(c->L_t) * c->k + o, n_sel * 4);
     if ((s = take_device_error(c)) != KVB_OK) return s;
     if (numeric) return fail(KVB_ERR_NUMERIC, "a single-source system was not positive definite");
     return KVB_OK;
@@ -485,8 +509,9 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
     if (!(lambda >= 0.0)) return fail(KVB_ERR_INVALID_ARG, "lambda must be >= 0");
     kvb_status s;
     SelTable tab;
-    if ((s = check_selection(c, sel_k_host, "sel_k", &tab, 0)) != KVB_OK) return s;
-    if ((s = check_selection(c, sel_v_host, "sel_v", &tab, 1)) != KVB_OK) return s;
+    const int t_end = st->t0 + st->nt;  // the statistics' target block
+    if ((s = check_selection(c, sel_k_host, "sel_k", &tab, 0, st->t0, t_end)) != KVB_OK) return s;
+    if ((s = check_selection(c, sel_v_host, "sel_v", &tab, 1, st->t0, t_end)) != KVB_OK) return s;
     if ((s = check_device_ptrs({W_k, W_v, b_k, b_v}, "kvb_ridge_solve")) != KVB_OK) return s;
     if ((s = take_device_error(c)) != KVB_OK) return s;
     DevGuard g(c->device);
@@ -494,7 +519,7 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
     const int q = c->H * c->d;
     const int64_t p = static_cast<int64_t>(c->k) * q;
     const size_t wes = w_dtype == KVB_F32 ? 4 : 2;
-    int B = static_cast<int>(std::min<int64_t>({MAX_SYS, c->L_t, std::max<int64_t>(1, WS_BUDGET / (p * p * 4))}));
+    int B = static_cast<int>(std::min<int64_t>({MAX_SYS, st->nt, std::max<int64_t>(1, WS_BUDGET / (p * p * 4))}));
     if ((s = ws_grow(st, &st->wsG, &st->wsG_bytes, size_t(B) * p * p * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsR, &st->wsR_bytes, size_t(B) * p * q * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsD, &st->wsD_bytes, size_t(B) * p * 4)) != KVB_OK) return s;
@@ -510,8 +535,8 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
     {
         ProfScope ps(c, cs, "ridge_solve");
         for (int kv = 0; kv < 2 && e == cudaSuccess; ++kv) {
-            for (int t0 = 0; t0 < c->L_t && e == cudaSuccess; t0 += B) {
-                const int nb = std::min(B, c->L_t - t0);
+            for (int t0 = st->t0; t0 < t_end && e == cudaSuccess; t0 += B) {
+                const int nb = std::min(B, t_end - t0);
                 SysLayers L;
                 SysOut O;
                 std::memset(&L, 0, sizeof(L));
@@ -519,7 +544,7 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
                 for (int b = 0; b < nb; ++b) {
                     const int t = t0 + b;
                     for (int j = 0; j < c->k; ++j) L.layer[b][j] = selh[kv][t * c->k + j];
-                    L.col0[b] = int64_t(t) * q;
+                    L.col0[b] = int64_t(t - st->t0) * q;  // column of the block's statistics
                     O.W[b] = static_cast<char*>(Wout[kv]) + size_t(t) * q * p * wes;
                     O.bias[b] = bout[kv] + size_t(t) * q;
                 }

@@ -188,6 +188,24 @@ kvb_status kvb_map_apply_noalloc(const kvb_model_spec* src, const kvb_model_spec
  */
 kvb_status kvb_stats_create(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_batch_tokens,
                             kvb_stats** out);
+
+/*
+ * Target-layer block ("KVBridge" README, "Loading": target-layer blocking
+ * bounds peak memory at the cost of more passes over the calibration data).
+ * The object holds the statistics of target layers [t_begin, t_end) only:
+ * the full-source Gram as above, but the cross statistics, target means and
+ * target sums of squares of the block's (t_end - t_begin)*H*d columns, so the
+ * memory is 4 * (L_src*H*d)^2 + 4 * L_src*H*d * (t_end - t_begin)*H*d bytes
+ * per kv instead of the full L_tgt*H*d columns.  kvb_stats_accumulate still
+ * takes the whole [L_tgt][H][T][d] target caches and reads the block's layers;
+ * kvb_layer_select writes (and kvb_ridge_solve reads) only the block's rows
+ * of the selections, R^2, W and b; export / import move the block's columns.
+ * A fit over all target layers runs one pass over the calibration data per
+ * block.  kvb_stats_create is the block [0, L_tgt).  Requires
+ * 0 <= t_begin < t_end <= L_tgt (else KVB_ERR_INVALID_ARG).
+ */
+kvb_status kvb_stats_create_block(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_batch_tokens,
+                                  int32_t t_begin, int32_t t_end, kvb_stats** out);
 kvb_status kvb_stats_destroy(kvb_stats* st);
 
 /* Zero the statistics (n = 0), asynchronously on `stream`. */

@@ -179,6 +179,50 @@ def test_bf16_tensor_core_statistics_head_dims_packed_short_sequences(kvb, d, H)
     _check_stats(kvb, st, pair, 1e-4)
 
 
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 16)])
+def test_target_layer_blocks_reproduce_the_full_fit(kvb, dtype, d):
+    # statistics of a target-layer block hold only that block's target columns;
+    # one calibration pass per block gives the selections, R^2 and maps of the
+    # object that holds every target layer
+    # 8 sequences x 512 tokens, stride 4: 1024 observations for 2 x 2 x d features
+    pair = make_pair(31, 4, 5, 2, d, 2, 512, 8, 1e4, 1e6, noise=1e-2, sigma=1.0)
+    if dtype == torch.bfloat16:
+        pair = round_pair(pair, torch.bfloat16)
+    code = kvb.KVB_BF16 if dtype == torch.bfloat16 else kvb.KVB_F32
+    ctx = _ctx(kvb, pair, 512)
+    L_t, L_s, k, q = 5, 4, 2, 2 * d
+    full = kvb.kvb_stats_create(ctx, code, 512)
+    _accumulate(kvb, ctx, full, pair["calib"], dtype)
+    sel_k, sel_v, r2, Wk, Wv, bk, bv = _run_fit(kvb, ctx, full, pair, torch.float32)
+    _, _, _, cross_full, _ = _export(kvb, full, 0, L_s * q, L_t * q)[1:]
+
+    bsk = np.zeros((L_t, k), dtype=np.int32)
+    bsv = np.zeros((L_t, k), dtype=np.int32)
+    br2 = torch.zeros((2, L_t, L_s), dtype=torch.float32, device="cuda")
+    bWk, bWv = torch.zeros_like(Wk), torch.zeros_like(Wv)
+    bbk, bbv = torch.zeros_like(bk), torch.zeros_like(bv)
+    for t0, t1 in ((0, 2), (2, 5)):
+        st = kvb.kvb_stats_create_block(ctx, code, 512, t0, t1)
+        _accumulate(kvb, ctx, st, pair["calib"], dtype)
+        n, _, _, _, cross_blk, _ = _export(kvb, st, 0, L_s * q, (t1 - t0) * q)
+        assert np.abs(cross_blk - cross_full[:, t0 * q:t1 * q]).max() <= 1e-5 * np.abs(cross_full).max()
+        kvb.kvb_layer_select(ctx, st, 0.01, br2, sel_k=bsk, sel_v=bsv)
+        kvb.kvb_ridge_solve(ctx, st, bsk, bsv, 0.01, bWk, bWv, bbk, bbv)
+        kvb.kvb_stats_destroy(st)
+    assert np.array_equal(bsk, sel_k) and np.array_equal(bsv, sel_v)
+    assert np.abs(to_host64(br2) - r2).max() <= 1e-5
+    for a, b in ((bWk, Wk), (bWv, Wv), (bbk, bk), (bbv, bv)):
+        assert rel_fro(to_host64(a), to_host64(b)) <= 1e-5
+
+
+def test_target_block_range_is_validated(kvb):
+    pair = make_pair(32, 3, 4, 2, 16, 2, 64, 1, 1e4, 1e6)
+    ctx = _ctx(kvb, pair, 64)
+    for t0, t1 in ((-1, 2), (2, 2), (3, 2), (0, 5)):
+        with pytest.raises(kvb.KvbError):
+            kvb.kvb_stats_create_block(ctx, kvb.KVB_F32, 64, t0, t1)
+
+
 def test_bad_calibration_position_is_reported(kvb):
     pair = make_pair(13, 3, 2, 2, 16, 2, 64, 1, 1e4, 1e6)
     ctx = _ctx(kvb, pair, 32)  # positions reach 63 >= max_pos

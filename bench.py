@@ -204,15 +204,17 @@ FIT = dict(L_s=40, L_t=64, H=8, d=128, k=8, seq_len=1024, n_seq=256, batch_token
 FIT_SMALL = dict(FIT, L_s=8, L_t=8, k=4, n_seq=32)
 
 
-def run_fit(kvb, dev, seed=101, small=False):
+def run_fit(kvb, dev, seed=101, small=False, block=0):
     """Calibration statistics + selection + ridge solve, Qwen3-14B->32B shapes.
 
     256 sequences x 1024 tokens (positions 0..1023) streamed in 32 batches of
     8192 tokens, stride 4 -> 65,536 observations.  Batch data: source caches
     drawn with the synthetic recipe; target caches produced from them by a
-    hidden top-8 affine map (applied with kvb_map_apply) plus noise at SNR 10.
-    Four distinct batches are generated and cycled (timing does not depend on
-    the values).  Returns a dict for the JSON line.
+    hidden top-8 affine map (applied with kvb_map_apply) plus noise at SNR 10;
+    every batch distinct, generated between the timed accumulate calls.  With
+    block > 0 the statistics hold `block` target layers at a time (bounded
+    memory) and every block re-streams the 32 batches.  Returns a dict for the
+    JSON line.
     """
     import torch
     import synth
@@ -237,6 +239,7 @@ def run_fit(kvb, dev, seed=101, small=False):
     tv = torch.empty_like(tk)
 
     def make_batch(b):
+        g.manual_seed(seed * 7919 + b)  # the same batch on every pass
         sk.copy_(synth.torch_content(seed + 10 + b, L_s, H, Tb, d, 1.0, torch.bfloat16, dev))
         sv.copy_(synth.torch_content(seed + 1000 + b, L_s, H, Tb, d, 1.0, torch.bfloat16, dev))
         kvb.kvb_map_apply(ctx, sk, sv, pos, sel_k, sel_v, Wk, Wv, bk, bv, tk, tv)
@@ -246,54 +249,66 @@ def run_fit(kvb, dev, seed=101, small=False):
                 x += torch.randn(x.shape, generator=g, device=dev) * (x.std(dim=1, keepdim=True) / F["snr"] ** 0.5)
                 t[l].copy_(x)
 
-    st = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, Tb)
     stream = torch.cuda.current_stream(dev)
     kvb.kvb_profile_read(ctx)
-    stats_ms = 0.0
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    kern = {}
-    for b in range(n_batches):  # every batch distinct; only the accumulate calls are timed
-        make_batch(b)
-        kvb.kvb_profile_enable(ctx, True)
-        e0.record(stream)
-        kvb.kvb_stats_accumulate(ctx, st, sk, sv, tk, tv, pos, F["stride"], stream)
-        e1.record(stream)
-        kvb.kvb_profile_enable(ctx, False)
-        torch.cuda.synchronize(dev)
-        stats_ms += e0.elapsed_time(e1)
-        for n, (c, t) in kvb.kvb_profile_read(ctx).items():
-            c0, t0_ = kern.get(n, (0, 0.0))
-            kern[n] = (c0 + c, t0_ + t)
-    del Wk, Wv, sk, sv, tk, tv
-    kvb.kvb_ctx_check(ctx, stream)
-    n_obs = kvb.kvb_stats_count(st, stream)
+    blocks = [(0, L_t)] if block <= 0 else [(t, min(t + block, L_t)) for t in range(0, L_t, block)]
+    gk = np.zeros((L_t, k), dtype=np.int32)
+    gv = np.zeros((L_t, k), dtype=np.int32)
     r2 = torch.empty((2, L_t, L_s), dtype=torch.float32, device=dev)
-    kvb.kvb_profile_enable(ctx, True)
-    t0 = time.perf_counter()
-    gk, gv = kvb.kvb_layer_select(ctx, st, F["lam"], r2, stream)
-    t_sel = time.perf_counter() - t0
     Wk_o = torch.empty((L_t, q, p), dtype=torch.bfloat16, device=dev)
     Wv_o = torch.empty_like(Wk_o)
     bk_o = torch.empty((L_t, q), dtype=torch.float32, device=dev)
     bv_o = torch.empty_like(bk_o)
-    t0 = time.perf_counter()
-    kvb.kvb_ridge_solve(ctx, st, gk, gv, F["lam"], Wk_o, Wv_o, bk_o, bv_o, stream)
-    t_ridge = time.perf_counter() - t0
-    kvb.kvb_profile_enable(ctx, False)
-    for n, (c, t) in kvb.kvb_profile_read(ctx).items():
-        kern[n] = (c, t)
+    stats_ms, t_sel, t_ridge = 0.0, 0.0, 0.0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kern = {}
+
+    def collect(into_sum):
+        for n, (c, t) in kvb.kvb_profile_read(ctx).items():
+            c0, t0_ = kern.get(n, (0, 0.0)) if into_sum else (0, 0.0)
+            kern[n] = (c0 + c, t0_ + t)
+
+    for t_begin, t_end in blocks:
+        st = kvb.kvb_stats_create_block(ctx, kvb.KVB_BF16, Tb, t_begin, t_end)
+        for b in range(n_batches):  # every batch distinct; only the accumulate calls are timed
+            make_batch(b)
+            kvb.kvb_profile_enable(ctx, True)
+            e0.record(stream)
+            kvb.kvb_stats_accumulate(ctx, st, sk, sv, tk, tv, pos, F["stride"], stream)
+            e1.record(stream)
+            kvb.kvb_profile_enable(ctx, False)
+            torch.cuda.synchronize(dev)
+            stats_ms += e0.elapsed_time(e1)
+            collect(True)
+        kvb.kvb_ctx_check(ctx, stream)
+        n_obs = kvb.kvb_stats_count(st, stream)
+        kvb.kvb_profile_enable(ctx, True)
+        t0 = time.perf_counter()
+        kvb.kvb_layer_select(ctx, st, F["lam"], r2, stream, sel_k=gk, sel_v=gv)
+        t_sel += time.perf_counter() - t0
+        t0 = time.perf_counter()
+        kvb.kvb_ridge_solve(ctx, st, gk, gv, F["lam"], Wk_o, Wv_o, bk_o, bv_o, stream)
+        t_ridge += time.perf_counter() - t0
+        kvb.kvb_profile_enable(ctx, False)
+        collect(True)
+        kvb.kvb_stats_destroy(st)
+    del Wk, Wv, sk, sv, tk, tv
     Fs, Ft = L_s * q, L_t * q
-    flop_alg = 2 * n_obs * (Fs * Fs / 2 + Fs * Ft) * 2       # lower Gram + cross, K and V
+    # lower Gram (once per pass) + cross (every target column once), K and V
+    flop_alg = 2 * n_obs * (len(blocks) * Fs * Fs / 2 + Fs * Ft) * 2
     gemm_name = "stats_gemm_tcgen05" if "stats_gemm_tcgen05" in kern else "stats_gemm_simt"
     gemm_n, gemm_ms = kern.get(gemm_name, (0, 0.0))
     gather_n, gather_ms = kern.get("calib_gather_center", (0, 0.0))
     nb = Tb // F["stride"]
     # algorithmic bytes: kept rows of the four caches read once, centered (hi, lo) operands written once
-    gather_bytes = n_batches * ((2 * L_s + 2 * L_t) * H * nb * d * 2 + (2 * Fs + 2 * Ft) * nb * 4)
+    gather_bytes = n_batches * (len(blocks) * (2 * L_s * H * nb * d * 2 + 2 * Fs * nb * 4) +
+                                2 * L_t * H * nb * d * 2 + 2 * Ft * nb * 4)
+    blk = max(t1 - t0 for t0, t1 in blocks)
     out = {"workload": (f"{L_s}->{L_t} layers, k={k}, " if small else "qwen3-14b->32b-shaped fit: ") +
                        f"{F['n_seq']} x {F['seq_len']} calibration tokens in {n_batches} batches of {Tb}, stride 4, "
                        "bf16 caches, fp32 statistics (split-bf16 tensor-core products), lambda 0.01",
-           "n_obs": n_obs, "batches": n_batches,
+           "n_obs": n_obs, "batches": n_batches, "target_block": blk, "passes": len(blocks),
+           "stats_bytes": 2 * 4 * (Fs * Fs + Fs * blk * q),
            "stats_ms": stats_ms, "stats_gemm_kernel": gemm_name, "stats_gemm_ms": gemm_ms,
            "stats_gemm_tflops_algorithmic": flop_alg / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
            "stats_gemm_tflops_executed": 3 * flop_alg / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
@@ -301,7 +316,7 @@ def run_fit(kvb, dev, seed=101, small=False):
            "select_s": t_sel, "ridge_s": t_ridge,
            "selection_recovered": float((np.asarray(gk) == sel_k).mean() + (np.asarray(gv) == sel_v).mean()) / 2,
            "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in kern.items()}}
-    del st, Wk_o, Wv_o
+    del Wk_o, Wv_o
     kvb.kvb_ctx_destroy(ctx)
     torch.cuda.empty_cache()
     return out
@@ -699,6 +714,8 @@ def main():
     ap.add_argument("--skip-fp32", action="store_true", help="skip the fp32-cache map leg")
     ap.add_argument("--fp32-only", action="store_true", help="run only the fp32-cache map leg")
     ap.add_argument("--fit-only", action="store_true", help="run only the fit leg (with --workload small: 8 -> 8 layers)")
+    ap.add_argument("--fit-block", type=int, default=0,
+                    help="fit leg with statistics of this many target layers at a time (one pass per block)")
     args = ap.parse_args()
     if args.workload == "small":
         W["T"] = 4096
@@ -722,7 +739,7 @@ def main():
         elif args.fp32_only:
             res = {"fp32_map": run_fp32_map(kvb, dev)}
         else:
-            res = {"fit": run_fit(kvb, dev, small=args.workload == "small")}
+            res = {"fit": run_fit(kvb, dev, small=args.workload == "small", block=args.fit_block)}
         if rank == 0:
             print(json.dumps(res), flush=True)
         return

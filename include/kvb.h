@@ -141,7 +141,10 @@ kvb_status kvb_profile_read(kvb_ctx* ctx, kvb_kernel_time* out, int32_t cap, int
  *   W_k/W_v     device [L_tgt][H*d][k*H*d]  (dtype)
  *   b_k/b_v     device [L_tgt][H*d] float32
  *   out_k/out_v device [L_tgt][H][T][d] (dtype), fully overwritten
- * T == 0 is a no-op.  Device pointers must be 16-byte aligned.
+ * T == 0 is a no-op.  Device pointers must be 16-byte aligned.  Calls on one
+ * context share its scratch (the stripped keys, the strip's work counters):
+ * issue them on one stream, or order them, never overlapping on the GPU; use
+ * one context per concurrent stream.
  */
 kvb_status kvb_map_apply(kvb_ctx* ctx, kvb_dtype dtype, const void* src_k, const void* src_v,
                          const int32_t* positions, int64_t T, const int32_t* sel_k,

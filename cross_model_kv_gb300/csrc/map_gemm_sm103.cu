@@ -207,13 +207,15 @@ __device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c
             if (valid && F32OUT) {
                 float* o = static_cast<float*>(P.out[c.kv]) + orow;
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const float4 a = bad_pos ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                             : make_float4(xl[4 * v], xl[4 * v + 1], xl[4 * v + 2], xl[4 * v + 3]);
-                    const float4 b = bad_pos ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                             : make_float4(xh[4 * v], xh[4 * v + 1], xh[4 * v + 2], xh[4 * v + 3]);
-                    *reinterpret_cast<float4*>(o + e0 + 4 * v) = a;
-                    *reinterpret_cast<float4*>(o + half + e0 + 4 * v) = b;
+                for (int v = 0; v < 2; ++v) {  // 8 outputs = one 32-byte sector per store
+                    uint32_t a[8], b[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        a[u] = bad_pos ? 0u : __float_as_uint(xl[8 * v + u]);
+                        b[u] = bad_pos ? 0u : __float_as_uint(xh[8 * v + u]);
+                    }
+                    st_global_v8(o + e0 + 8 * v, a);
+                    st_global_v8(o + half + e0 + 8 * v, b);
                 }
             } else if (valid) {
                 __nv_bfloat16* o = static_cast<__nv_bfloat16*>(P.out[c.kv]) + orow;
@@ -223,10 +225,8 @@ __device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c
                     pl[v] = bad_pos ? 0u : pack_bf16x2(xl[2 * v], xl[2 * v + 1]);
                     ph[v] = bad_pos ? 0u : pack_bf16x2(xh[2 * v], xh[2 * v + 1]);
                 }
-                st_global_v4(o + e0, make_uint4(pl[0], pl[1], pl[2], pl[3]));
-                st_global_v4(o + e0 + 8, make_uint4(pl[4], pl[5], pl[6], pl[7]));
-                st_global_v4(o + half + e0, make_uint4(ph[0], ph[1], ph[2], ph[3]));
-                st_global_v4(o + half + e0 + 8, make_uint4(ph[4], ph[5], ph[6], ph[7]));
+                st_global_v8(o + e0, pl);  // 16 outputs = one 32-byte sector
+                st_global_v8(o + half + e0, ph);
             }
         }
     }

@@ -404,12 +404,6 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// One 32-byte global store (sm_100 and later); p must be 32-byte aligned.
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(p), "r"(w[0]), "r"(w[1]),
-                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-}
 
 // Threads of the streaming gather: every thread keeps 16 rows of one RoPE pair.
 __host__ __device__ constexpr int stream_threads(int d) { return kChunk * (d / 2) / 16; }

@@ -214,15 +214,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN + colhalf * 128);
-            float4 cur[4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) cur[v] = *reinterpret_cast<const float4*>(orow + 4 * v);
+            // 16 statistics per step as two 32-byte (one-sector) accesses; the next step's
+            // values are loaded before this step's accumulator is read
+            uint32_t cur[2][8];
+            ld_global_v8(orow, cur[0]);
+            ld_global_v8(orow + 8, cur[1]);
 #pragma unroll 1
             for (int c0 = 0; c0 < 128; c0 += 16) {
-                float4 nxt[4];
+                uint32_t nxt[2][8];
                 if (c0 + 16 < 128) {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) nxt[v] = *reinterpret_cast<const float4*>(orow + c0 + 16 + 4 * v);
+                    ld_global_v8(orow + c0 + 16, nxt[0]);
+                    ld_global_v8(orow + c0 + 24, nxt[1]);
                 }
                 uint32_t r[16];
                 if (iters > 0) {
@@ -233,19 +235,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int v = 0; v < 16; ++v) r[v] = 0u;
                 }
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const float4 d = __ldg(reinterpret_cast<const float4*>(dbp + c0 + 4 * v));
-                    const float4 z = __ldg(reinterpret_cast<const float4*>(zbp + c0 + 4 * v));
-                    float4 o = cur[v];
-                    o.x += __uint_as_float(r[4 * v + 0]) + fda * d.x - gza * z.x;
-                    o.y += __uint_as_float(r[4 * v + 1]) + fda * d.y - gza * z.y;
-                    o.z += __uint_as_float(r[4 * v + 2]) + fda * d.z - gza * z.z;
-                    o.w += __uint_as_float(r[4 * v + 3]) + fda * d.w - gza * z.w;
-                    *reinterpret_cast<float4*>(orow + c0 + 4 * v) = o;
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t o[8];
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        const float4 d = __ldg(reinterpret_cast<const float4*>(dbp + c0 + 8 * h + 4 * v));
+                        const float4 z = __ldg(reinterpret_cast<const float4*>(zbp + c0 + 8 * h + 4 * v));
+                        const float dd[4] = {d.x, d.y, d.z, d.w}, zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int e = 4 * v + u;
+                            o[e] = __float_as_uint(__uint_as_float(cur[h][e]) + __uint_as_float(r[8 * h + e]) +
+                                                   fda * dd[u] - gza * zz[u]);
+                        }
+                    }
+                    st_global_v8(orow + c0 + 8 * h, o);
                 }
                 if (c0 + 16 < 128) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) cur[v] = nxt[v];
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) cur[h][e] = nxt[h][e];
                 }
             }
             if (iters > 0) {

@@ -172,7 +172,7 @@ kvb_status kvb_ctx_create(const kvb_model_spec* src, const kvb_model_spec* tgt, 
         if ((e = cudaMalloc(&c->tab_s, tab_bytes)) != cudaSuccess) { st = cuda_fail(e, "cudaMalloc rope table"); break; }
         if ((e = cudaMalloc(&c->tab_t, tab_bytes)) != cudaSuccess) { st = cuda_fail(e, "cudaMalloc rope table"); break; }
         if ((e = cudaMalloc(&c->err_dev, sizeof(int))) != cudaSuccess) { st = cuda_fail(e, "cudaMalloc error word"); break; }
-        if ((e = cudaMalloc(&c->strip_ctr, 2 * sizeof(int))) != cudaSuccess) { st = cuda_fail(e, "cudaMalloc counters"); break; }
+        if ((e = cudaMalloc(&c->strip_ctr, 4 * sizeof(int))) != cudaSuccess) { st = cuda_fail(e, "cudaMalloc counters"); break; }
         if ((e = cudaHostAlloc(&c->err_mirror, sizeof(int), cudaHostAllocDefault)) != cudaSuccess) { st = cuda_fail(e, "cudaHostAlloc"); break; }
         *c->err_mirror = 0;
         if ((e = cudaMemset(c->err_dev, 0, sizeof(int))) != cudaSuccess) { st = cuda_fail(e, "cudaMemset"); break; }
@@ -258,9 +258,8 @@ kvb_status kvb_map_apply(kvb_ctx* c, kvb_dtype dtype, const void* src_k, const v
         // keys while the value tiles are computed) unless KVB_MAP_FUSED_STRIP=0.
         const char* fs = std::getenv("KVB_MAP_FUSED_STRIP");
         const bool fused = !(fs && std::strcmp(fs, "0") == 0) && map_gemm_fused_strip_supported(sh);
-        if (fused) {
-            e = cudaMemsetAsync(c->strip_ctr, 0, 2 * sizeof(int), s);
-        } else {
+        e = cudaMemsetAsync(c->strip_ctr, 0, 4 * sizeof(int), s);  // strip and tile counters
+        if (e == cudaSuccess && !fused) {
             ProfScope ps(c, s, "rope_strip_bf16");
             e = launch_strip_bf16(static_cast<const __nv_bfloat16*>(src_k), static_cast<__nv_bfloat16*>(c->scratch),
                                   positions, c->tab_s, static_cast<int64_t>(c->L_s) * c->H, T, c->d, c->max_pos,
@@ -275,6 +274,8 @@ kvb_status kvb_map_apply(kvb_ctx* c, kvb_dtype dtype, const void* src_k, const v
             a.tab_s = c->tab_s;
             a.strip_ctr = c->strip_ctr;
         }
+        const char* ps = std::getenv("KVB_MAP_PAIR_STATIC");  // fixed tiles per pair (comparison runs)
+        a.tile_ctr = (ps && std::strcmp(ps, "1") == 0) ? nullptr : c->strip_ctr + 2;
         a.a_src[0] = c->scratch;
         a.a_src[1] = src_v;
         a.w[0] = W_k;

@@ -19,7 +19,7 @@ struct kvb_ctx {
     void* scratch = nullptr;   // stripped source keys for the tensor-core path
     size_t scratch_bytes = 0;
     int* err_dev = nullptr;    // error word written by kernels
-    int* strip_ctr = nullptr;  // [2]: next / finished chunk of the strip fused into the map kernel
+    int* strip_ctr = nullptr;  // [4]: next / finished chunk of the strip fused into the map kernel, next map tile
     int* err_mirror = nullptr; // pinned host copy, refreshed after each call
     // kernel timing (kvb_profile_enable / kvb_profile_read)
     struct ProfRec {

@@ -61,6 +61,7 @@ struct MapGemmArgs {
     const void* k_raw;      // [L_s*H][T][d] bf16 source keys as stored
     const float2* tab_s;    // source RoPE table
     int* strip_ctr;         // [2] zeroed before the launch
+    int* tile_ctr;          // CTA-pair kernel: tile claim counter zeroed before the launch, or null (fixed tiles)
     const float* bias[2];   // [L_t][q]
     void* out[2];           // [L_t][H][T][d] bf16 (fp32 when split)
     const int* pos;

@@ -7,16 +7,21 @@
 // ships").  The feature matrix is never materialised: each 64-wide K-block of
 // X_t is one token-block x 64-dim box of one (layer, head) slab of the source
 // cache, fetched by TMA at coordinates (e0, token0, sel*H + h).  For K the
-// source operand is the RoPE-stripped copy written by the strip pass.
+// source operand is the RoPE-stripped copy of the keys, which the kernel's own
+// epilogue warps write while the value tiles run (or a separate strip pass).
 //
 // Two persistent, warp-specialised kernels share the epilogue:
-//   map_gemm_kernel      one CTA per SM, tiles of 128 tokens x 256 outputs,
-//                        tcgen05.mma cta_group::1 (M=128 N=256 K=16);
 //   map_gemm_pair_kernel clusters of 2 CTAs on 2 SMs, tiles of 256 tokens x
 //                        256 outputs, tcgen05.mma cta_group::2 (M=256 N=256):
 //                        each CTA stages its own 128 token rows and half of
 //                        the 256 output rows of W, so a stage is 32 KB per SM
-//                        instead of 48 KB and six stages fit instead of four.
+//                        instead of 48 KB and six stages fit instead of four;
+//                        tiles are claimed in order from a global counter.
+//                        The bf16 default.
+//   map_gemm_kernel      one CTA per SM, tiles of 128 tokens x 256 outputs,
+//                        tcgen05.mma cta_group::1 (M=128 N=256 K=16), tiles
+//                        assigned round-robin; fp32 caches, and bf16 with
+//                        KVB_MAP_PAIR=0.
 // Roles: warp 0 TMA producer (one lane), warp 1 MMA issuer (one lane; in the
 // pair kernel only the even CTA issues), warps 2..5 epilogue: TMEM ->
 // registers, + bias, target RoPE for K (pairs (e, e+64) of one head are in the
@@ -61,7 +66,7 @@ constexpr int PSTAGES = KVB_MAP_PAIR_STAGES;
 constexpr int PA_BYTES = 128 * BK * 2;
 constexpr int PB_BYTES = 128 * BK * 2;
 constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
-constexpr int PSMEM_BYTES = PSTAGES * PSTAGE_BYTES + 1024 + 256;
+constexpr int PSMEM_BYTES = PSTAGES * PSTAGE_BYTES + 1024 + 512;
 
 struct Params {
     int L_t, H, d, T, num_m, num_n, nk, total_tiles, max_pos;
@@ -80,6 +85,7 @@ struct Params {
     int* strip_ctr;              // [0] next chunk to claim, [1] chunks finished
     int strip_chunks;            // chunks of 128 tokens per (layer, head) slab
     int strip_items;             // all chunks
+    int* tile_ctr;               // CTA-pair kernel: next tile to claim (zeroed before the launch), or null
 };
 
 struct TileCoord {
@@ -137,6 +143,44 @@ __device__ __forceinline__ void strip_chunk(const Params& P, int item, int lane)
         *reinterpret_cast<uint4*>(P.k_strip + o) = olo;
         *reinterpret_cast<uint4*>(P.k_strip + o + half) = ohi;
     }
+}
+
+// Producer, before the first key tile: every chunk of the stripped keys has been
+// written (by any CTA), bounded like every other wait; then the TMA loads see the
+// generic-proxy writes.  False on timeout or abort.
+__device__ __forceinline__ bool wait_strip_done(const Params& P, volatile int* abort_flag) {
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire_gpu(P.strip_ctr + 1) < P.strip_items) {
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > P.err.timeout_ns) {
+            dev_err_set(P.err, DEV_ERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+        __nanosleep(256);
+    }
+    fence_proxy_async_global();
+    return true;
+}
+
+// Epilogue warp: while the accumulator is not ready, strip chunks of the source
+// keys.  Returns false once no chunk is left to claim (warp-uniform).
+__device__ __forceinline__ bool strip_while_waiting(const Params& P, uint64_t* tfull, uint32_t parity, int lane,
+                                                    volatile int* abort_flag) {
+    while (!__any_sync(0xffffffffu, mbar_try_wait(tfull, parity))) {
+        int item = 0;
+        if (lane == 0) item = *abort_flag ? P.strip_items : atomicAdd(P.strip_ctr, 1);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item >= P.strip_items) return false;
+        strip_chunk(P, item, lane);
+        fence_proxy_async_global();  // for the TMA loads of other CTAs
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence();  // the warp's stores before the count (release)
+            atomicAdd(P.strip_ctr + 1, 1);
+        }
+    }
+    return true;
 }
 
 // K-block kb of target layer t: (source layer, head, first dim) of its box.
@@ -309,24 +353,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
                 const TileCoord c = decode_tile(P, tile);
                 if (c.kv == 0 && !stripped) {
-                    // every chunk of the stripped keys is written (by any CTA) before
-                    // the first key tile is loaded; bounded like every other wait
-                    const uint64_t t0 = global_timer_ns();
-                    while (ld_acquire_gpu(P.strip_ctr + 1) < P.strip_items) {
-                        if (*abort_flag) {
-                            ok = false;
-                            break;
-                        }
-                        if (global_timer_ns() - t0 > P.err.timeout_ns) {
-                            dev_err_set(P.err, DEV_ERR_TIMEOUT);
-                            *abort_flag = 1;
-                            ok = false;
-                            break;
-                        }
-                        __nanosleep(256);
-                    }
-                    if (!ok) break;
-                    fence_proxy_async_global();  // the TMA loads below see the generic-proxy writes
+                    if (!wait_strip_done(P, abort_flag)) break;
                     stripped = true;
                 }
                 for (int ki = 0; ki < nk_issue; ++ki) {
@@ -404,23 +431,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool strip_left = P.fuse_strip != 0;  // warp-uniform
         for (int tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x) {
             const TileCoord c = decode_tile(P, tile);
-            // while the accumulator is not ready, strip chunks of the source keys
-            while (strip_left && !__any_sync(0xffffffffu, mbar_try_wait(&tfull[acc], acc_phase))) {
-                int item = 0;
-                if (lane == 0) item = *abort_flag ? P.strip_items : atomicAdd(P.strip_ctr, 1);
-                item = __shfl_sync(0xffffffffu, item, 0);
-                if (item >= P.strip_items) {
-                    strip_left = false;
-                    break;
-                }
-                strip_chunk(P, item, lane);
-                fence_proxy_async_global();  // for the TMA loads of other CTAs
-                __syncwarp();
-                if (lane == 0) {
-                    __threadfence();  // the warp's stores before the count (release)
-                    atomicAdd(P.strip_ctr + 1, 1);
-                }
-            }
+            if (strip_left) strip_left = strip_while_waiting(P, &tfull[acc], acc_phase, lane, abort_flag);
             if (!mbar_wait(&tfull[acc], acc_phase, P.err, abort_flag)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
@@ -448,6 +459,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // accumulator rows of its tokens.  Both CTAs' copies complete on rank 0's
 // `full` barrier; rank 0 issues the pair MMAs and commits to both CTAs'
 // `empty` / `tfull` barriers; both CTAs' epilogues arrive on rank 0's `tempty`.
+//
+// Tiles are handed out in index order from a global counter (P.tile_ctr):
+// rank 0's producer claims the next tile and passes its index through a ring
+// of PRING slots in both CTAs' shared memory (sfull / sempty barriers) to the
+// MMA issuer, both epilogues and rank 1's producer.  The four tiles of one
+// token block (consecutive indices) therefore start together on four pairs,
+// which read the block's source rows while they are in L2; a fixed
+// tile-per-pair assignment lets the pairs drift apart by several tiles over a
+// launch and re-read them from DRAM.  With tile_ctr == nullptr the same ring
+// carries the fixed assignment pair, pair + npairs, ...
+constexpr int PRING = 4;
+constexpr int SCHED_CONSUMERS = 1 + 4 + 1 + 4;  // MMA, epilogue warps of rank 0, producer and epilogue warps of rank 1
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     map_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                          const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
@@ -462,7 +486,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* tfull = empty + PSTAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* sfull = drain + 1;
+    uint64_t* sempty = sfull + PRING;
+    volatile int* ring = reinterpret_cast<volatile int*>(sempty + PRING);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(ring + PRING));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -482,6 +509,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&tempty[a], 2 * 128);
         }
         mbar_init(drain, 1);
+        for (int r = 0; r < PRING; ++r) {
+            mbar_init(&sfull[r], 1);
+            mbar_init(&sempty[r], SCHED_CONSUMERS);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -501,6 +532,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     const int q = P.H * P.d;
+    // a consumer's release of a ring slot, on rank 0's sempty
+    auto release_slot = [&](int slot) { mbar_arrive_cluster(mapa_shared(smem_u32(&sempty[slot]), 0)); };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -509,9 +542,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int issued_phase[PSTAGES];
             for (int s = 0; s < PSTAGES; ++s) issued_phase[s] = -1;
+            int slot = 0;
+            uint32_t sphase = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
+            bool stripped = !P.fuse_strip;
+            for (int claim = 0; ok; ++claim) {
+                int tile;
+                if (leader) {
+                    // claim the next tile and publish it to both CTAs
+                    if (!mbar_wait<true>(&sempty[slot], sphase ^ 1u, P.err, abort_flag)) break;
+                    tile = P.tile_ctr ? atomicAdd(P.tile_ctr, 1) : pair + claim * npairs;
+                    if (tile > P.total_tiles) tile = P.total_tiles;  // every index past the end is the stop mark
+                    ring[slot] = tile;
+                    st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(ring + slot)), 1),
+                                          static_cast<uint32_t>(tile));
+                    mbar_arrive(&sfull[slot]);
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&sfull[slot]), 1));
+                } else {
+                    if (!mbar_wait<true>(&sfull[slot], sphase, P.err, abort_flag)) break;
+                    tile = ring[slot];
+                    release_slot(slot);
+                }
+                if (++slot == PRING) {
+                    slot = 0;
+                    sphase ^= 1u;
+                }
+                if (tile >= P.total_tiles) break;
                 const TileCoord c = decode_tile(P, tile);
+                if (c.kv == 0 && !stripped) {
+                    if (!wait_strip_done(P, abort_flag)) break;
+                    stripped = true;
+                }
                 const CUtensorMap* ta = c.kv ? &tm_a1 : &tm_a0;
                 const CUtensorMap* tw = c.kv ? &tm_w1 : &tm_w0;
                 for (int kb = 0; kb < P.nk; ++kb) {
@@ -547,8 +608,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
+            int slot = 0;
+            uint32_t sphase = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < P.total_tiles; tile += npairs) {
+            while (ok) {
+                if (!mbar_wait<true>(&sfull[slot], sphase, P.err, abort_flag)) break;
+                const int tile = ring[slot];
+                release_slot(slot);
+                if (++slot == PRING) {
+                    slot = 0;
+                    sphase ^= 1u;
+                }
+                if (tile >= P.total_tiles) break;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, P.err, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -585,8 +656,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = sub * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = pair; tile < P.total_tiles; tile += npairs) {
+        int slot = 0;
+        uint32_t sphase = 0;
+        bool strip_left = P.fuse_strip != 0;  // warp-uniform
+        for (;;) {
+            if (!mbar_wait<true>(&sfull[slot], sphase, P.err, abort_flag)) break;
+            const int tile = ring[slot];
+            __syncwarp();
+            if (lane == 0) release_slot(slot);
+            if (++slot == PRING) {
+                slot = 0;
+                sphase ^= 1u;
+            }
+            if (tile >= P.total_tiles) break;
             const TileCoord c = decode_tile(P, tile);
+            if (strip_left) strip_left = strip_while_waiting(P, &tfull[acc], acc_phase, lane, abort_flag);
             if (!mbar_wait(&tfull[acc], acc_phase, P.err, abort_flag)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
@@ -628,9 +712,10 @@ bool encode_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, 
     return true;
 }
 
+// The CTA-pair kernel serves bf16 caches unless KVB_MAP_PAIR=0 (single-CTA kernel).
 bool use_pair_kernel() {
     const char* s = std::getenv("KVB_MAP_PAIR");
-    return s && std::strcmp(s, "1") == 0;
+    return !(s && std::strcmp(s, "0") == 0);
 }
 
 }  // namespace
@@ -641,7 +726,7 @@ bool map_gemm_tc_supported(const Shape& sh) {
 }
 
 bool map_gemm_fused_strip_supported(const Shape& sh) {
-    return map_gemm_tc_supported(sh) && !use_pair_kernel() &&
+    return map_gemm_tc_supported(sh) &&
            static_cast<int64_t>(sh.L_s) * sh.H * ((sh.T + 127) / 128) < 0x7fffffffLL;
 }
 
@@ -660,7 +745,7 @@ cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string
     P.num_n = q / BN;
     P.nk = p / BK;
     const int64_t total = 2LL * sh.L_t * P.num_m * P.num_n;
-    if (total > 0x7fffffffLL) {
+    if (total > 0x7fffffffLL - 4096) {  // the pair kernel's claims run a few past the last tile
         if (why) *why = "too many tiles";
         return cudaErrorInvalidValue;
     }
@@ -679,6 +764,7 @@ cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string
         P.strip_chunks = static_cast<int>((sh.T + 127) / 128);
         P.strip_items = static_cast<int>(static_cast<int64_t>(sh.L_s) * sh.H * P.strip_chunks);
     }
+    P.tile_ctr = pair ? a.tile_ctr : nullptr;
     for (int kv = 0; kv < 2; ++kv) {
         P.bias[kv] = a.bias[kv];
         P.out[kv] = a.out[kv];

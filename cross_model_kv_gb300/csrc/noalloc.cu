@@ -79,7 +79,7 @@ extern "C" kvb_status kvb_map_apply_noalloc(const kvb_model_spec* src, const kvb
     if (!map_gemm_tc_supported(sh))
         return fail(KVB_ERR_UNSUPPORTED, "kvb_map_apply_noalloc needs head_dim 128 and n_kv_heads * 128 a multiple of 256");
 
-    // Scratch layout: [source table | target table | stripped keys | error word].
+    // Scratch layout: [source table | target table | stripped keys | error word, tile counter].
     const size_t tab_bytes = align256(size_t(max_pos) * (sh.d / 2) * sizeof(float2));
     const size_t keys_bytes = align256(size_t(sh.L_s) * sh.H * size_t(T) * sh.d * 2);
     const size_t need = 2 * tab_bytes + keys_bytes + 256;
@@ -124,8 +124,8 @@ extern "C" kvb_status kvb_map_apply_noalloc(const kvb_model_spec* src, const kvb
     const DevErr err{err_word, timeout_ns};
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
-    // The error word must start at zero; the tables and keys are fully rewritten.
-    e = cudaMemsetAsync(err_word, 0, sizeof(int), cs);
+    // The error word and the tile counter start at zero; the tables and keys are fully rewritten.
+    e = cudaMemsetAsync(err_word, 0, 2 * sizeof(int), cs);
     if (e == cudaSuccess) e = launch_rope_table(tab_s, max_pos, sh.d, src->rope_theta, cs);
     if (e == cudaSuccess) e = launch_rope_table(tab_t, max_pos, sh.d, tgt->rope_theta, cs);
     if (e == cudaSuccess)
@@ -147,6 +147,7 @@ extern "C" kvb_status kvb_map_apply_noalloc(const kvb_model_spec* src, const kvb
     a.sel = tab;
     a.err = err;
     a.num_sms = num_sms;
+    a.tile_ctr = err_word + 1;
     std::string why;
     e = launch_map_gemm_tc(a, cs, &why);
     if (e != cudaSuccess) {

@@ -3,6 +3,7 @@
 Small cases compare every element; the full-size pair shapes compare sampled
 target layers x sampled tokens (rows and layers are independent, so the
 oracle on a slice is exact for that slice)."""
+import os
 import numpy as np
 import pytest
 
@@ -135,6 +136,37 @@ def test_fused_and_separate_strip_give_identical_bits(kvb, monkeypatch):
     ok, ov = c.oracle([0, 3], None)
     gk, gv = c.gpu([0, 3], None)
     assert rel_fro(gk, ok) <= TOL_BF16 and rel_fro(gv, ov) <= TOL_BF16
+
+
+@pytest.mark.parametrize("shape", ["ragged_two_n_tiles", "qwen3_0p6b_to_1p7b_T4096"])
+def test_pair_kernel_schedules_and_single_cta_kernel(kvb, monkeypatch, shape):
+    # bf16 maps run on CTA pairs with tiles claimed from a counter; the same pair kernel
+    # with the fixed tile-per-pair assignment (KVB_MAP_PAIR_STATIC=1) computes every
+    # tile identically, and the single-CTA kernel (KVB_MAP_PAIR=0) is checked on its own
+    if shape == "ragged_two_n_tiles":
+        c = ApplyCase(5, 4, 4, 128, 2, 1500, 1e4, 1e6, torch.bfloat16, seed=39)
+        layers, tokens, max_pos = None, None, 1500
+    else:
+        c = ApplyCase(28, 28, 8, 128, 4, 4096, 1e6, 1e6, torch.bfloat16, seed=40, host=False)
+        layers, tokens, max_pos = [0, 27], _sampled_tokens(4096, 256, 5), 4096
+    ctx = _ctx(kvb, c, max_pos)
+    ok, ov = c.oracle(layers, tokens)
+    outs = {}
+    for name, env in [("dynamic", {}), ("static", {"KVB_MAP_PAIR_STATIC": "1"}), ("single", {"KVB_MAP_PAIR": "0"})]:
+        for k in ("KVB_MAP_PAIR_STATIC", "KVB_MAP_PAIR"):
+            monkeypatch.delenv(k, raising=False)
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        c.out_k.zero_()
+        c.out_v.zero_()
+        c.run(kvb, ctx)
+        kvb.kvb_ctx_check(ctx)
+        outs[name] = (c.out_k.clone(), c.out_v.clone())
+        gk, gv = c.gpu(layers, tokens)
+        assert rel_fro(gk, ok) <= TOL_BF16 and rel_fro(gv, ov) <= TOL_BF16, name
+    assert torch.equal(outs["dynamic"][0], outs["static"][0]) and torch.equal(outs["dynamic"][1], outs["static"][1])
+    del c, outs
+    torch.cuda.empty_cache()
 
 
 def test_empty_input_is_a_no_op(kvb):

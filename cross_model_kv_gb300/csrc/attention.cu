@@ -318,7 +318,7 @@ extern "C" kvb_status kvb_attention_cosine(kvb_ctx* c, kvb_dtype dtype, const vo
     P.scale = 1.f / sqrtf(static_cast<float>(d));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (attn_tc_supported(dtype, d, T) && T <= 0x7fffffffLL) {
+    if (attn_tc_supported(dtype, d, T, static_cast<int64_t>(c->L_t) * n_q_heads * Tq)) {
         std::string why;
         {
             ProfScope ps(c, s, "attention_cosine_tcgen05");

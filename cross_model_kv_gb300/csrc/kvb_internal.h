@@ -91,8 +91,9 @@ struct MapSimtArgs {
 };
 cudaError_t launch_map_simt(const MapSimtArgs& a, cudaStream_t s);
 
-// Attention-output cosine on the tensor cores (bf16 caches, head_dim 128, T >= 1).
-bool attn_tc_supported(kvb_dtype dtype, int d, int64_t T);
+// Attention-output cosine on the tensor cores (bf16 caches, head_dim 128, 1 <= T < 2^31,
+// fewer than 2^31 query rows L * Hq * Tq).
+bool attn_tc_supported(kvb_dtype dtype, int d, int64_t T, int64_t q_rows);
 cudaError_t launch_attn_cosine_tc(const void* q, const int* q_pos, const void* k_a, const void* v_a, const void* k_b,
                                   const void* v_b, const int* kv_pos, float* cos_out, int L, int H, int Hq, int Tq,
                                   int64_t T, DevErr err, cudaStream_t s, std::string* why);

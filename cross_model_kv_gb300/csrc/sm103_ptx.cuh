@@ -176,7 +176,22 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: BF16 x BF16 -> F32, both operands K-major.
+// Shared-memory matrix descriptor: MN-major operand, 128-byte swizzle.  Each
+// 128-byte row holds 64 consecutive MN elements of one K index; 8-row (K)
+// groups are 1024 bytes apart (stride offset) and the next 64 MN elements start
+// `mn_stride` bytes further (leading offset).
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t mn_stride) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);          // start address  [0,14)
+    d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;  // leading offset [16,30)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;                   // stride offset  [32,46)
+    d |= static_cast<uint64_t>(1) << 46;                           // descriptor version [46,48)
+    d |= static_cast<uint64_t>(2) << 61;                           // swizzle: 128B  [61,64)
+    return d;
+}
+
+// Instruction descriptor, kind::f16: BF16 x BF16 -> F32, both operands K-major
+// (OR in IDESC_B_MN for an MN-major B operand).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
     return (1u << 4)             // D format F32      [4,6)
            | (1u << 7)           // A format BF16     [7,10)
@@ -184,6 +199,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
            | ((N >> 3) << 17)    // N / 8             [17,23)
            | ((M >> 4) << 24);   // M / 16            [24,29)
 }
+constexpr uint32_t IDESC_B_MN = 1u << 16;  // B operand MN-major (transpose B)
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {

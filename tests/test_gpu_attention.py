@@ -109,6 +109,20 @@ def test_unsorted_positions_mask_by_position_not_index(kvb):
     assert np.all(got[:, :, q_pos < 0] == 0)
 
 
+def test_tensor_core_unsorted_positions_partial_row_blocks(kvb):
+    # bf16, head_dim 128 (tensor-core kernel): permuted key positions over three key
+    # tiles (the last partial), queries that see nothing, part or all of the keys, and
+    # 3 x 45 = 135 query rows (a second, almost empty row block)
+    rng = np.random.default_rng(98)
+    kv_pos = rng.permutation(300)
+    q_pos = np.concatenate([[-5, 0, 299, 1000], rng.integers(0, 300, size=41)])
+    c = Case(98, L=2, H=2, g=3, d=128, T=300, Tq=45, dtype=torch.bfloat16, q_pos=q_pos, kv_pos=kv_pos)
+    got = c.gpu(kvb, _ctx(kvb, 2, 2, 128))
+    ref = c.oracle()
+    assert np.abs(got - ref).max() <= TOL_COS
+    assert np.all(got[:, :, q_pos < 0] == 0)
+
+
 def test_identical_caches_give_one(kvb):
     c = Case(92, L=1, H=2, g=2, d=128, T=130, Tq=130, dtype=torch.bfloat16, noise=0.0)
     got = c.gpu(kvb, _ctx(kvb, 1, 2, 128))

@@ -210,11 +210,19 @@ __device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c
     const int heads_per_tile = BN / P.d;
     const float* bias = P.bias[c.kv] + static_cast<int64_t>(c.t) * q + c.n * BN;
     const float2* tab = P.tab_t + static_cast<int64_t>(p) * half;
-    for (int hh = 0; hh < heads_per_tile; ++hh) {
-        const int h = c.n * heads_per_tile + hh;
-        const int64_t orow = ((static_cast<int64_t>(c.t) * P.H + h) * P.T + tok) * P.d;
+    // 16 RoPE pairs at a time; their (cos, sin) serve every head of the tile
 #pragma unroll 1
-        for (int e0 = 0; e0 < half; e0 += 16) {
+    for (int e0 = 0; e0 < half; e0 += 16) {
+        float4 cs[8];
+        if (c.kv == 0) {
+            const float4* tp = reinterpret_cast<const float4*>(tab + e0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) cs[v] = __ldg(tp + v);  // (c, s) of pairs 2v and 2v+1
+        }
+#pragma unroll 1
+        for (int hh = 0; hh < heads_per_tile; ++hh) {
+            const int h = c.n * heads_per_tile + hh;
+            const int64_t orow = ((static_cast<int64_t>(c.t) * P.H + h) * P.T + tok) * P.d;
             uint32_t lo[16], hi[16];
             tmem_ld16(tbase + hh * P.d + e0, lo);
             tmem_ld16(tbase + hh * P.d + half + e0, hi);
@@ -236,16 +244,14 @@ __device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c
                 xh[4 * v + 3] = __uint_as_float(hi[4 * v + 3]) + b.w;
             }
             if (c.kv == 0) {
-                const float4* tp = reinterpret_cast<const float4*>(tab + e0);
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
-                    const float4 cs = __ldg(tp + v);  // (c, s) of pairs 2v and 2v+1
                     const float l0 = xl[2 * v], h0 = xh[2 * v];
                     const float l1 = xl[2 * v + 1], h1 = xh[2 * v + 1];
-                    xl[2 * v] = fmaf(l0, cs.x, -(h0 * cs.y));
-                    xh[2 * v] = fmaf(h0, cs.x, l0 * cs.y);
-                    xl[2 * v + 1] = fmaf(l1, cs.z, -(h1 * cs.w));
-                    xh[2 * v + 1] = fmaf(h1, cs.z, l1 * cs.w);
+                    xl[2 * v] = fmaf(l0, cs[v].x, -(h0 * cs[v].y));
+                    xh[2 * v] = fmaf(h0, cs[v].x, l0 * cs[v].y);
+                    xl[2 * v + 1] = fmaf(l1, cs[v].z, -(h1 * cs[v].w));
+                    xh[2 * v + 1] = fmaf(h1, cs[v].z, l1 * cs[v].w);
                 }
             }
             if (valid && F32OUT) {

@@ -344,6 +344,10 @@ kvb_status kvb_map_apply(kvb_ctx* c, kvb_dtype dtype, const void* src_k, const v
         a.sel = tab;
         a.err = dev_err(c);
         a.num_sms = c->num_sms;
+        const char* ps_env = std::getenv("KVB_MAP_PAIR_STATIC");  // fixed tiles per pair (comparison runs)
+        a.tile_ctr = (ps_env && std::strcmp(ps_env, "1") == 0) ? nullptr : c->strip_ctr + 2;
+        e = cudaMemsetAsync(c->strip_ctr, 0, 4 * sizeof(int), s);
+        if (e != cudaSuccess) return cuda_fail(e, "counter reset");
         std::string why;
         {
             ProfScope ps(c, s, "map_gemm_tcgen05_split3");

@@ -17,18 +17,17 @@
 //                        the 256 output rows of W, so a stage is 32 KB per SM
 //                        instead of 48 KB and six stages fit instead of four;
 //                        tiles are claimed in order from a global counter.
-//                        The bf16 default.
+//                        The default.
 //   map_gemm_kernel      one CTA per SM, tiles of 128 tokens x 256 outputs,
 //                        tcgen05.mma cta_group::1 (M=128 N=256 K=16), tiles
-//                        assigned round-robin; fp32 caches, and bf16 with
-//                        KVB_MAP_PAIR=0.
+//                        assigned round-robin; with KVB_MAP_PAIR=0.
 // Roles: warp 0 TMA producer (one lane), warp 1 MMA issuer (one lane; in the
 // pair kernel only the even CTA issues), warps 2..5 epilogue: TMEM ->
 // registers, + bias, target RoPE for K (pairs (e, e+64) of one head are in the
 // same tile), round to bf16, store straight into the target cache
 // [t][h][token][e].  Accumulators are double buffered in TMEM (2 x 256 columns).
-// fp32 caches run through the single-CTA kernel with each operand carried as
-// a bf16 (hi, lo) pair and an fp32 output (map_gemm_kernel<true>).
+// fp32 caches run through the same kernels with each operand carried as a
+// bf16 (hi, lo) pair and an fp32 output (SPLIT = true).
 // Every wait is bounded (DevErr::timeout_ns); on expiry the CTA records
 // DEV_ERR_TIMEOUT, stops, drains its copies and MMAs and frees TMEM.
 #include <cstdlib>
@@ -478,10 +477,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 constexpr int PRING = 4;
 constexpr int SCHED_CONSUMERS = 1 + 4 + 1 + 4;  // MMA, epilogue warps of rank 0, producer and epilogue warps of rank 1
 
+// SPLIT as in the single-CTA kernel: fp32 operands as bf16 (hi, lo) pairs, three
+// products per 64-wide K block, fp32 output.
+template <bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     map_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                          const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+                         const __grid_constant__ CUtensorMap tm_a0l, const __grid_constant__ CUtensorMap tm_a1l,
+                         const __grid_constant__ CUtensorMap tm_w0l, const __grid_constant__ CUtensorMap tm_w1l,
                          const __grid_constant__ Params P) {
+    constexpr int NSEG = SPLIT ? 3 : 1;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -527,6 +532,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tm_a1);
         tma_prefetch_desc(&tm_w0);
         tma_prefetch_desc(&tm_w1);
+        if (SPLIT) {
+            tma_prefetch_desc(&tm_a0l);
+            tma_prefetch_desc(&tm_a1l);
+            tma_prefetch_desc(&tm_w0l);
+            tma_prefetch_desc(&tm_w1l);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -579,9 +590,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!wait_strip_done(P, abort_flag)) break;
                     stripped = true;
                 }
-                const CUtensorMap* ta = c.kv ? &tm_a1 : &tm_a0;
-                const CUtensorMap* tw = c.kv ? &tm_w1 : &tm_w0;
-                for (int kb = 0; kb < P.nk; ++kb) {
+                for (int ki = 0; ki < P.nk * NSEG; ++ki) {
+                    const int kb = SPLIT ? ki / 3 : ki;
+                    const int seg = SPLIT ? ki - 3 * kb : 0;  // 0: hi x hi, 1: hi x lo, 2: lo x hi
+                    const CUtensorMap* ta = seg == 2 ? (c.kv ? &tm_a1l : &tm_a0l) : (c.kv ? &tm_a1 : &tm_a0);
+                    const CUtensorMap* tw = seg == 1 ? (c.kv ? &tm_w1l : &tm_w0l) : (c.kv ? &tm_w1 : &tm_w0);
                     if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) {
                         ok = false;
                         break;
@@ -629,7 +642,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, P.err, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < P.nk; ++kb) {
+                for (int kb = 0; kb < P.nk * NSEG; ++kb) {
                     if (!mbar_wait(&full[stage], phase, P.err, abort_flag)) {
                         ok = false;
                         break;
@@ -680,7 +693,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!mbar_wait(&tfull[acc], acc_phase, P.err, abort_flag)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            epilogue_row<false>(P, c, c.m * PM + 128 * static_cast<int>(rank) + row, tbase, q);
+            epilogue_row<SPLIT>(P, c, c.m * PM + 128 * static_cast<int>(rank) + row, tbase, q);
             tc_fence_before();
             mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
             acc ^= 1;
@@ -740,7 +753,7 @@ cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string
     const Shape& sh = a.sh;
     const int q = sh.H * sh.d;
     const int p = sh.k * q;
-    const bool pair = !a.split && use_pair_kernel() && a.num_sms >= 2;
+    const bool pair = use_pair_kernel() && a.num_sms >= 2;
     const int tm = pair ? PM : BM;
     Params P{};
     P.L_t = sh.L_t;
@@ -784,7 +797,8 @@ cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string
             if (!encode_3d_bf16(&tmal[kv], a.a_lo[kv], sh.d, sh.T, static_cast<uint64_t>(sh.L_s) * sh.H, BK, 128,
                                 why))
                 return cudaErrorInvalidValue;
-            if (!encode_3d_bf16(&tmwl[kv], a.w_lo[kv], p, q, sh.L_t, BK, BN, why)) return cudaErrorInvalidValue;
+            if (!encode_3d_bf16(&tmwl[kv], a.w_lo[kv], p, q, sh.L_t, BK, pair ? 128 : BN, why))
+                return cudaErrorInvalidValue;
         } else {
             tmal[kv] = tma[kv];  // unused by the bf16 kernel
             tmwl[kv] = tmw[kv];
@@ -799,7 +813,8 @@ cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string
                                                    P);
         return cudaGetLastError();
     }
-    cudaError_t e = cudaFuncSetAttribute(map_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PSMEM_BYTES);
+    auto pkern = a.split ? map_gemm_pair_kernel<true> : map_gemm_pair_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(pkern, cudaFuncAttributeMaxDynamicSharedMemorySize, PSMEM_BYTES);
     if (e != cudaSuccess) return e;
     int pairs = a.num_sms / 2;
     if (total < pairs) pairs = static_cast<int>(total);
@@ -815,7 +830,7 @@ cudaError_t launch_map_gemm_tc(const MapGemmArgs& a, cudaStream_t s, std::string
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, map_gemm_pair_kernel, tma[0], tma[1], tmw[0], tmw[1], P);
+    e = cudaLaunchKernelEx(&cfg, pkern, tma[0], tma[1], tmw[0], tmw[1], tmal[0], tmal[1], tmwl[0], tmwl[1], P);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -138,14 +138,19 @@ def test_fused_and_separate_strip_give_identical_bits(kvb, monkeypatch):
     assert rel_fro(gk, ok) <= TOL_BF16 and rel_fro(gv, ov) <= TOL_BF16
 
 
-@pytest.mark.parametrize("shape", ["ragged_two_n_tiles", "qwen3_0p6b_to_1p7b_T4096"])
+@pytest.mark.parametrize("shape", ["ragged_two_n_tiles", "ragged_two_n_tiles_fp32", "qwen3_0p6b_to_1p7b_T4096"])
 def test_pair_kernel_schedules_and_single_cta_kernel(kvb, monkeypatch, shape):
-    # bf16 maps run on CTA pairs with tiles claimed from a counter; the same pair kernel
-    # with the fixed tile-per-pair assignment (KVB_MAP_PAIR_STATIC=1) computes every
-    # tile identically, and the single-CTA kernel (KVB_MAP_PAIR=0) is checked on its own
+    # maps run on CTA pairs with tiles claimed from a counter (bf16, and fp32 caches as
+    # bf16 hi/lo parts); the same pair kernel with the fixed tile-per-pair assignment
+    # (KVB_MAP_PAIR_STATIC=1) computes every tile identically, and the single-CTA
+    # kernel (KVB_MAP_PAIR=0) is checked on its own
+    tol = TOL_BF16
     if shape == "ragged_two_n_tiles":
         c = ApplyCase(5, 4, 4, 128, 2, 1500, 1e4, 1e6, torch.bfloat16, seed=39)
         layers, tokens, max_pos = None, None, 1500
+    elif shape == "ragged_two_n_tiles_fp32":
+        c = ApplyCase(5, 4, 4, 128, 2, 700, 1e4, 1e6, torch.float32, seed=41)
+        layers, tokens, max_pos, tol = None, None, 700, TOL_F32
     else:
         c = ApplyCase(28, 28, 8, 128, 4, 4096, 1e6, 1e6, torch.bfloat16, seed=40, host=False)
         layers, tokens, max_pos = [0, 27], _sampled_tokens(4096, 256, 5), 4096
@@ -163,7 +168,7 @@ def test_pair_kernel_schedules_and_single_cta_kernel(kvb, monkeypatch, shape):
         kvb.kvb_ctx_check(ctx)
         outs[name] = (c.out_k.clone(), c.out_v.clone())
         gk, gv = c.gpu(layers, tokens)
-        assert rel_fro(gk, ok) <= TOL_BF16 and rel_fro(gv, ov) <= TOL_BF16, name
+        assert rel_fro(gk, ok) <= tol and rel_fro(gv, ov) <= tol, name
     assert torch.equal(outs["dynamic"][0], outs["static"][0]) and torch.equal(outs["dynamic"][1], outs["static"][1])
     del c, outs
     torch.cuda.empty_cache()

@@ -160,6 +160,27 @@ def test_bf16_fit_matches_oracle(kvb):
     _check_fit(kvb, ctx, st, pair, torch.float32, TOL_W)
 
 
+def test_statistics_on_cta_pairs_and_single_ctas_agree(kvb, monkeypatch):
+    # sizes that are multiples of 256 run on CTA pairs (256 x 256 tiles) unless
+    # KVB_STATS_PAIR=0 when the statistics are created; both merge the same sums
+    pair = round_pair(make_pair(12, 4, 3, 2, 128, 2, 1024, 6, 1e4, 1e6, noise=1e-2, sigma=1.0), torch.bfloat16)
+    ctx = _ctx(kvb, pair, 1024)
+    st_pair = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, 1024)
+    monkeypatch.setenv("KVB_STATS_PAIR", "0")
+    st_one = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, 1024)
+    monkeypatch.delenv("KVB_STATS_PAIR")
+    for st in (st_pair, st_one):
+        _accumulate(kvb, ctx, st, pair["calib"], torch.bfloat16)
+        _check_stats(kvb, st, pair, 1e-4)
+    q = pair["H"] * pair["d"]
+    for kv in (0, 1):
+        a = _export(kvb, st_pair, kv, pair["L_s"] * q, pair["L_t"] * q)
+        b = _export(kvb, st_one, kv, pair["L_s"] * q, pair["L_t"] * q)
+        assert a[0] == b[0]
+        for x, y in zip(a[1:], b[1:]):
+            assert rel_fro(x, y) <= 1e-6
+
+
 @pytest.mark.parametrize("d,H", [(32, 8), (64, 4), (16, 16)])
 def test_bf16_tensor_core_statistics_head_dims_packed_short_sequences(kvb, d, H):
     # H*d = 256, so the statistics run on the tensor cores; the single-pass gather

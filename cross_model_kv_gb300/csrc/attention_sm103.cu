@@ -18,11 +18,12 @@
 //                K 128), then, once the probabilities are written,
 //                O += P_hi V + P_lo V with V read MN-major straight from the
 //                TMA tile;
-//   warps 4..7 / 8..11  softmax of cache a / b, one query row per thread: S
-//                from TMEM (two passes: the masked tile maximum, then the
-//                probabilities), P as a bf16 pair (hi, lo: ~16 significant
-//                bits) into shared memory in the operand layout (hi over the
-//                consumed key tile).
+//   warps 4..11 / 12..19  softmax of cache a / b, two threads per query row
+//                (64 keys and 64 output dims each): S from TMEM (two passes:
+//                the masked tile maximum, exchanged between the row's two
+//                threads, then the probabilities), P as a bf16 pair (hi, lo:
+//                ~16 significant bits) into shared memory in the operand
+//                layout (hi over the consumed key tile).
 // Exponentials are taken against a running reference maximum that is only
 // raised (and O rescaled in TMEM) when a tile's maximum exceeds it by more than
 // 2^8, so most tiles need no rescale; the softmax denominators cancel in the
@@ -43,7 +44,7 @@ constexpr int TK = 128;                 // keys per tile
 constexpr int HD = 128;                 // head dim
 constexpr int ATOM = 128 * 128;         // bytes of a 128-row x 64-element bf16 swizzle block
 constexpr int TILE = 2 * ATOM;          // 128 x 128 bf16
-constexpr int NUM_THREADS = 384;
+constexpr int NUM_THREADS = 640;
 constexpr int MAX_FLAG_TILES = 1024;
 constexpr int SMEM_BYTES = 7 * TILE + 1024 + 256 + MAX_FLAG_TILES;
 constexpr uint64_t DRAIN_NS = 200ull * 1000 * 1000;
@@ -139,10 +140,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&kv_full[x], 1);
             mbar_init(&kv_empty[x], 1);
             mbar_init(&s_full[x], 1);
-            mbar_init(&p_full[x], 128);
+            mbar_init(&p_full[x], 256);
             mbar_init(&drain[x], 1);
         }
-        mbar_init(b_done, 128);
+        mbar_init(b_done, 256);
         mbar_init(q_full, 1);
         *abort_flag = 0;
         *qmax_s = INT_MIN;
@@ -164,12 +165,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
 
     // the rows' positions and the CTA's smallest and largest
-    const int gx = (warp - 4) >> 2;          // softmax warpgroup: cache index
+    const int gx = (warp - 4) >> 3;          // softmax warps: cache index
+    const int hf = ((warp - 4) >> 2) & 1;    // softmax warps: which 64 keys / output dims of the row
     const int row = 32 * (warp & 3) + lane;  // softmax warps: TMEM lane = tile row
     const int grow = r0 + row;
     const bool valid = warp >= 4 && grow < rows;
     const int qp = valid ? __ldg(P.q_pos + grow % P.Tq) : INT_MIN;
-    if (valid && gx == 0) {
+    if (valid && gx == 0 && hf == 0) {
         atomicMax(qmax_s, qp);
         atomicMin(qmin_s, qp);
     }
@@ -241,9 +243,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // ----------------------------------------------------------- softmax, cache gx
+        // Two threads per row (warps w and w + 4 share a TMEM lane quarter): this one
+        // takes keys kh0 .. kh0+63 of every tile and output dims kh0 .. kh0+63.  The two
+        // halves exchange tile maxima (and, at the end, the cosine's sums) through the
+        // cache's P-lo tile, which no MMA reads at those points.  The eight warps of a
+        // cache meet at named barrier 1 + x; whether to go on is agreed there first
+        // (every wait before it is bounded), so no warp leaves while others wait.
         const int x = gx;
+        const int kh0 = 64 * hf;
+        const int bar_id = 1 + x;
         const uint32_t tl = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-        const uint32_t cS = 128u * x, cO = 256u + 128u * x;
+        const uint32_t cS = 128u * x + kh0, cO = 256u + 128u * x + kh0;
+        float* xch = reinterpret_cast<float*>(sPl(x));  // [2][128] exchange slots
         auto wait_all = [&](uint64_t* b, uint32_t parity) {  // warp-uniform outcome
             const bool got = mbar_wait(b, parity, P.err, abort_flag);
             return __all_sync(0xffffffffu, got);
@@ -253,52 +264,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         for (int t = 0; t < ntiles; ++t) {
             if (!live(t)) continue;
-            const int j0 = t * TK;
-            // visibility of the tile's keys for this row, while the MMA computes S:
+            const int j0 = t * TK + kh0;
+            // visibility of this thread's 64 keys, while the MMA computes S:
             // bit u of vis[w] is key j0 + 32 w + u
-            uint32_t vis[4] = {0u, 0u, 0u, 0u};
+            uint32_t vis[2] = {0u, 0u};
             if (use_flags && flags[t] == 2) {
-                if (valid) vis[0] = vis[1] = vis[2] = vis[3] = 0xffffffffu;
+                if (valid) vis[0] = vis[1] = 0xffffffffu;
             } else {
 #pragma unroll
-            for (int u = 0; u < TK; u += 4) {
-                const int4 p4 = key_pos4(P, j0 + u);
-                const int pa[4] = {p4.x, p4.y, p4.z, p4.w};
+                for (int u = 0; u < 64; u += 4) {
+                    const int4 p4 = key_pos4(P, j0 + u);
+                    const int pa[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
-                for (int w = 0; w < 4; ++w)
-                    // positions past the end are INT_MAX; a query at INT_MAX is
-                    // excluded from them by the index test
-                    if (valid && pa[w] <= qp && j0 + u + w < P.T) vis[u >> 5] |= 1u << ((u + w) & 31);
+                    for (int w = 0; w < 4; ++w)
+                        // positions past the end are INT_MAX; a query at INT_MAX is
+                        // excluded from them by the index test
+                        if (valid && pa[w] <= qp && j0 + u + w < P.T) vis[u >> 5] |= 1u << ((u + w) & 31);
+                }
             }
-            }
-            if (!wait_all(&s_full[x], it & 1)) {
-                ok = false;
-                break;
-            }
+            ok = named_bar_and(bar_id, 256, wait_all(&s_full[x], it & 1));
+            if (!ok) break;
             tc_fence_after();
-            // pass 1: the masked tile maximum, 64 columns per TMEM round trip
+            // pass 1: the masked maximum of this half row
             float mt = -INFINITY;
 #pragma unroll 1
-            for (int c0 = 0; c0 < TK; c0 += 64) {
-                uint32_t sv[4][16];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld16(tl + cS + c0 + 16 * c, sv[c]);
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t sv[2][16];
+                tmem_ld16(tl + cS + c0, sv[0]);
+                tmem_ld16(tl + cS + c0 + 16, sv[1]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 2; ++c)
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
-                        const int k = c0 + 16 * c + u;
-                        if ((vis[k >> 5] >> (k & 31)) & 1u) mt = fmaxf(mt, __uint_as_float(sv[c][u]));
+                        const int kk = c0 + 16 * c + u;
+                        if ((vis[kk >> 5] >> (kk & 31)) & 1u) mt = fmaxf(mt, __uint_as_float(sv[c][u]));
                     }
             }
-            mt *= P.scale_log2;  // scale > 0: the maximum commutes with it
+            xch[hf * 128 + row] = mt;
+            named_bar_sync(bar_id, 256);
+            mt = fmaxf(mt, xch[(1 - hf) * 128 + row]) * P.scale_log2;  // scale > 0: commutes with the maximum
+            named_bar_sync(bar_id, 256);  // both halves read before P lo overwrites the slots
             const bool raise = mt > m_ref + RESCALE_LOG2;  // also the first visible tile of the row
             if (__any_sync(0xffffffffu, raise && it > 0 && m_ref > -INFINITY)) {
-                // O was accumulated against the old reference: rescale it in TMEM
+                // O was accumulated against the old reference: rescale this half in TMEM
                 const float f = (raise && m_ref > -INFINITY) ? ex2_approx(m_ref - mt) : 1.f;
 #pragma unroll 1
-                for (int c0 = 0; c0 < HD; c0 += 16) {
+                for (int c0 = 0; c0 < 64; c0 += 16) {
                     uint32_t o[16];
                     tmem_ld16(tl + cO + c0, o);
                     tmem_ld_wait();
@@ -309,26 +321,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_st_wait();
             }
             if (raise) m_ref = mt;
-            // pass 2: probabilities as bf16 (hi, lo) in the operand layout; a tile that
-            // every row of the warp sees whole needs no per-key test
-            const bool all_vis = __all_sync(0xffffffffu, (vis[0] & vis[1] & vis[2] & vis[3]) == 0xffffffffu);
+            // pass 2: probabilities as bf16 (hi, lo) in the operand layout; keys that every
+            // row of the warp sees need no per-key test
+            const bool all_vis = __all_sync(0xffffffffu, (vis[0] & vis[1]) == 0xffffffffu);
 #pragma unroll 1
-            for (int c0 = 0; c0 < TK; c0 += 64) {
-                uint32_t sv[4][16];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld16(tl + cS + c0 + 16 * c, sv[c]);
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t sv[2][16];
+                tmem_ld16(tl + cS + c0, sv[0]);
+                tmem_ld16(tl + cS + c0 + 16, sv[1]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     float p[16];
                     if (all_vis) {
 #pragma unroll
-                        for (int u = 0; u < 16; ++u) p[u] = ex2_approx(fmaf(__uint_as_float(sv[c][u]), P.scale_log2, -m_ref));
+                        for (int u = 0; u < 16; ++u)
+                            p[u] = ex2_approx(fmaf(__uint_as_float(sv[c][u]), P.scale_log2, -m_ref));
                     } else {
 #pragma unroll
                         for (int u = 0; u < 16; ++u) {
-                            const int k = c0 + 16 * c + u;
-                            p[u] = ((vis[k >> 5] >> (k & 31)) & 1u)
+                            const int kk = c0 + 16 * c + u;
+                            p[u] = ((vis[kk >> 5] >> (kk & 31)) & 1u)
                                        ? ex2_approx(fmaf(__uint_as_float(sv[c][u]), P.scale_log2, -m_ref))
                                        : 0.f;
                         }
@@ -344,7 +357,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             hi[w] = *reinterpret_cast<const uint32_t*>(&bh);
                             lo[w] = pack_bf16x2(a - bf.x, b - bf.y);
                         }
-                        const uint32_t off = sw_off(row, (c0 >> 3) + 2 * c + h);
+                        const uint32_t off = sw_off(row, ((kh0 + c0) >> 3) + 2 * c + h);
                         *reinterpret_cast<uint4*>(sK(x) + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                         *reinterpret_cast<uint4*>(sPl(x) + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
@@ -355,24 +368,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive(&p_full[x]);
             ++it;
         }
-        // the cache's last O += P V is complete
-        if (ok && it > 0) ok = wait_all(&kv_empty[x], static_cast<uint32_t>((it - 1) & 1));
+        // the cache's last O += P V is complete (every warp waits; the outcome is agreed below)
+        bool fin = ok && (it == 0 || wait_all(&kv_empty[x], static_cast<uint32_t>((it - 1) & 1)));
         if (x == 1) {
-            if (ok && lane == 0 && warp == 8) *b_ok = 1;  // read by cache a's warps after b_done
+            fin = named_bar_and(bar_id, 256, fin);
+            if (fin && lane == 0 && warp == 12) *b_ok = 1;  // read by cache a's warps after b_done
             __syncwarp();
             tc_fence_before();
             mbar_arrive(b_done);  // also on failure, so that cache a's warps do not wait it out
         } else {
-            ok = ok && wait_all(b_done, 0) && *b_ok;
-            if (ok) {
+            fin = fin && wait_all(b_done, 0);
+            fin = named_bar_and(bar_id, 256, fin && *b_ok);
+            if (fin) {
                 tc_fence_after();
                 float dot = 0.f, na = 0.f, nb = 0.f;
                 if (it > 0) {
 #pragma unroll 1
-                    for (int c0 = 0; c0 < HD; c0 += 16) {
+                    for (int c0 = 0; c0 < 64; c0 += 16) {
                         uint32_t oa[16], ob[16];
-                        tmem_ld16(tl + 256u + c0, oa);
-                        tmem_ld16(tl + 384u + c0, ob);
+                        tmem_ld16(tl + 256u + kh0 + c0, oa);
+                        tmem_ld16(tl + 384u + kh0 + c0, ob);
                         tmem_ld_wait();
 #pragma unroll
                         for (int u = 0; u < 16; ++u) {
@@ -383,7 +398,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 }
-                if (valid) {
+                // the upper half's sums to the lower half (the P-lo tile is idle now)
+                if (hf == 1) {
+                    xch[row] = dot;
+                    xch[128 + row] = na;
+                    xch[256 + row] = nb;
+                }
+                named_bar_sync(bar_id, 256);
+                if (hf == 0 && valid) {
+                    dot += xch[row];
+                    na += xch[128 + row];
+                    nb += xch[256 + row];
                     const float den = sqrtf(na) * sqrtf(nb);
                     const int hq = kh * g + grow / P.Tq;
                     P.cos_out[(static_cast<int64_t>(l) * P.Hq + hq) * P.Tq + grow % P.Tq] = den > 0.f ? dot / den : 0.f;

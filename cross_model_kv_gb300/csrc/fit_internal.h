@@ -5,7 +5,7 @@
 
 namespace kvb {
 
-constexpr int MAX_SYS = 16;  // systems solved together in one batch
+constexpr int MAX_SYS = 64;  // systems solved together in one batch (every target layer of a 64-layer model)
 
 // Feature blocks of each system: system b uses source layers layer[b][0..k) (each
 // q = H*d features wide) and target columns col0[b] .. col0[b] + m.

@@ -61,7 +61,17 @@ struct kvb_stats {
 
 namespace {
 
-constexpr size_t WS_BUDGET = size_t(4) << 30;  // bytes of solve workspace per batch
+// Bytes of solve workspace per batch of systems: half the free device memory,
+// between 4 and 32 GiB (more systems per batch keep more SMs busy in the
+// panel steps of the factorisations, which work one diagonal block at a time).
+size_t ws_budget() {
+    size_t free_b = 0, total_b = 0;
+    if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
+        cudaGetLastError();
+        free_b = 0;
+    }
+    return std::max<size_t>(size_t(4) << 30, std::min<size_t>(size_t(32) << 30, free_b / 2));
+}
 
 kvb_status st_alloc(kvb_stats* st, void** p, size_t bytes) {
     cudaError_t e = cudaMalloc(p, bytes ? bytes : 16);
@@ -437,8 +447,9 @@ kvb_status kvb_layer_select(kvb_ctx* c, kvb_stats* st, double lambda, int32_t* s
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int q = c->H * c->d;
     const int64_t Ft = st->Ft;
+    const int64_t budget = static_cast<int64_t>(ws_budget());
     int B = static_cast<int>(std::min<int64_t>({MAX_SYS, c->L_s,
-                                                std::max<int64_t>(1, WS_BUDGET / (static_cast<int64_t>(q) * Ft * 4))}));
+                                                std::max<int64_t>(1, budget / (static_cast<int64_t>(q) * Ft * 4))}));
     if ((s = ws_grow(st, &st->wsG, &st->wsG_bytes, size_t(B) * q * q * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsR, &st->wsR_bytes, size_t(B) * q * Ft * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsD, &st->wsD_bytes, size_t(B) * q * 4)) != KVB_OK) return s;
@@ -519,7 +530,8 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
     const int q = c->H * c->d;
     const int64_t p = static_cast<int64_t>(c->k) * q;
     const size_t wes = w_dtype == KVB_F32 ? 4 : 2;
-    int B = static_cast<int>(std::min<int64_t>({MAX_SYS, st->nt, std::max<int64_t>(1, WS_BUDGET / (p * p * 4))}));
+    const int64_t budget = static_cast<int64_t>(ws_budget());
+    int B = static_cast<int>(std::min<int64_t>({MAX_SYS, st->nt, std::max<int64_t>(1, budget / (p * p * 4))}));
     if ((s = ws_grow(st, &st->wsG, &st->wsG_bytes, size_t(B) * p * p * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsR, &st->wsR_bytes, size_t(B) * p * q * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsD, &st->wsD_bytes, size_t(B) * p * 4)) != KVB_OK) return s;

@@ -656,6 +656,11 @@ def run_gpu(args, rank, world, local_rank):
     flop = FLOP_PER_TOKEN * T
     achieved = flop / (gemm_avg / 1000.0) / 1e12
     peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    # nominal dense bf16 peak of this device: SMs x 8192 bf16 flop per clock per SM
+    # (4096 tcgen05 kind::f16 FMAs) x the maximum SM clock the GPU reports
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    max_mhz = clk.get("sm_max_mhz") if isinstance(clk, dict) else None
+    nominal = n_sms * 8192 * max_mhz * 1e6 / 1e12 if max_mhz else None
     strip_bytes = 2 * (L_s * H * T * d * 2)
     strip_gbs = strip_bytes / (strip_avg / 1000.0) / 1e9 if strip_avg > 0 else None
 
@@ -673,6 +678,9 @@ def run_gpu(args, rank, world, local_rank):
                      "unit": "TFLOP/s", "frac": achieved / peak_sus,
                      "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a multi-second loop)",
                      "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
+                     "nominal_peak": nominal, "frac_of_nominal_peak": achieved / nominal if nominal else None,
+                     "nominal_basis": (f"{n_sms} SMs x 8192 bf16 flop/clock x {max_mhz} MHz (device maximum SM clock)"
+                                       if nominal else None),
                      "algorithmic_flop_per_launch": flop, "avg_launch_ms": gemm_avg,
                      "traffic": kernel_traffic(GEMM_KERNEL)},
         "hbm_pass": {"kernel": STRIP_KERNEL, "bound": "hbm", "achieved": strip_gbs, "peak": peaks["hbm_gbs"],

@@ -62,7 +62,7 @@ struct kvb_stats {
 namespace {
 
 // Bytes of solve workspace per batch of systems: half the free device memory,
-// between 4 and 32 GiB (more systems per batch keep more SMs busy in the
+// between 4 and 48 GiB (more systems per batch keep more SMs busy in the
 // panel steps of the factorisations, which work one diagonal block at a time).
 size_t ws_budget() {
     size_t free_b = 0, total_b = 0;
@@ -70,7 +70,7 @@ size_t ws_budget() {
         cudaGetLastError();
         free_b = 0;
     }
-    return std::max<size_t>(size_t(4) << 30, std::min<size_t>(size_t(32) << 30, free_b / 2));
+    return std::max<size_t>(size_t(4) << 30, std::min<size_t>(size_t(48) << 30, free_b / 2));
 }
 
 kvb_status st_alloc(kvb_stats* st, void** p, size_t bytes) {
@@ -447,9 +447,14 @@ kvb_status kvb_layer_select(kvb_ctx* c, kvb_stats* st, double lambda, int32_t* s
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int q = c->H * c->d;
     const int64_t Ft = st->Ft;
+    // The K and V systems of every source layer go through the factorisation and
+    // the solves together, as many per batch as the workspace budget holds.
+    const int n_sys = 2 * c->L_s;
+    const int64_t lq0 = ((q + 63) / 64) * 64 * 64;
+    const int64_t per_sys = 4 * (int64_t(q) * Ft + int64_t(q) * q + lq0 + Ft + q) +
+                            static_cast<int64_t>(tc_update_ws_bytes(q, Ft, 1));
     const int64_t budget = static_cast<int64_t>(ws_budget());
-    int B = static_cast<int>(std::min<int64_t>({MAX_SYS, c->L_s,
-                                                std::max<int64_t>(1, budget / (static_cast<int64_t>(q) * Ft * 4))}));
+    int B = static_cast<int>(std::min<int64_t>(n_sys, std::max<int64_t>(1, budget / per_sys)));
     if ((s = ws_grow(st, &st->wsG, &st->wsG_bytes, size_t(B) * q * q * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsR, &st->wsR_bytes, size_t(B) * q * Ft * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsD, &st->wsD_bytes, size_t(B) * q * 4)) != KVB_OK) return s;
@@ -462,27 +467,42 @@ kvb_status kvb_layer_select(kvb_ctx* c, kvb_stats* st, double lambda, int32_t* s
     const float lam = static_cast<float>(lambda);
     {
         ProfScope ps(c, cs, "r2_single_source");
-        for (int kv = 0; kv < 2 && e == cudaSuccess; ++kv) {
-            for (int s0 = 0; s0 < c->L_s && e == cudaSuccess; s0 += B) {
-                const int nb = std::min(B, c->L_s - s0);
-                SysLayers L;
-                std::memset(&L, 0, sizeof(L));
-                for (int b = 0; b < nb; ++b) L.layer[b][0] = s0 + b;
-                e = launch_gather_system(st->gram[kv], st->Fs, L, q, q, lam, st->wsG, int64_t(q) * q, st->wsD, nb, cs);
-                if (e == cudaSuccess)
-                    e = launch_gather_rhs(st->cross[kv], Ft, L, q, q, Ft, st->wsD, st->wsR, int64_t(q) * Ft, nb, cs);
-                if (e == cudaSuccess)
-                    e = chol_factor_batched(st->wsG, q, int64_t(q) * q, q, nb, st->numeric, st->wsL, lq, &tc, cs);
-                if (e == cudaSuccess)
-                    e = chol_solve_batched(st->wsG, q, int64_t(q) * q, q, st->wsL, lq, st->wsR, Ft, int64_t(q) * Ft, Ft,
-                                           nb, &tc, cs);
-                if (e == cudaSuccess)
-                    e = launch_sse(st->cross[kv], Ft, L, q, q, Ft, st->wsD, st->wsR, int64_t(q) * Ft, st->syy[kv], lam,
-                                   st->wsS, nb, cs);
-                if (e == cudaSuccess)
-                    e = launch_r2_head(st->wsS, Ft, st->syy[kv], st->nt, c->H, c->d, L,
-                                       st->r2 + (size_t(kv) * c->L_t + st->t0) * c->L_s, c->L_s, nb, cs);
-            }
+        for (int s0 = 0; s0 < n_sys && e == cudaSuccess; s0 += B) {
+            const int nb = std::min(B, n_sys - s0);
+            // the batch's systems of one cache at a time (system i: kv i / L_s, source
+            // layer i % L_s), at most MAX_SYS per launch of the per-system kernels
+            auto slices = [&](auto&& fn) {
+                for (int a = 0; a < nb && e == cudaSuccess;) {
+                    const int kv = (s0 + a) / c->L_s;
+                    const int end = std::min({nb, (kv + 1) * c->L_s - s0, a + MAX_SYS});
+                    SysLayers L;
+                    std::memset(&L, 0, sizeof(L));
+                    for (int b = a; b < end; ++b) L.layer[b - a][0] = (s0 + b) % c->L_s;
+                    e = fn(kv, static_cast<size_t>(a), end - a, L);
+                    a = end;
+                }
+            };
+            slices([&](int kv, size_t o, int cnt, const SysLayers& L) {
+                cudaError_t r = launch_gather_system(st->gram[kv], st->Fs, L, q, q, lam, st->wsG + o * q * q,
+                                                     int64_t(q) * q, st->wsD + o * q, cnt, cs);
+                if (r == cudaSuccess)
+                    r = launch_gather_rhs(st->cross[kv], Ft, L, q, q, Ft, st->wsD + o * q, st->wsR + o * q * Ft,
+                                          int64_t(q) * Ft, cnt, cs);
+                return r;
+            });
+            if (e == cudaSuccess)
+                e = chol_factor_batched(st->wsG, q, int64_t(q) * q, q, nb, st->numeric, st->wsL, lq, &tc, cs);
+            if (e == cudaSuccess)
+                e = chol_solve_batched(st->wsG, q, int64_t(q) * q, q, st->wsL, lq, st->wsR, Ft, int64_t(q) * Ft, Ft, nb,
+                                       &tc, cs);
+            slices([&](int kv, size_t o, int cnt, const SysLayers& L) {
+                cudaError_t r = launch_sse(st->cross[kv], Ft, L, q, q, Ft, st->wsD + o * q, st->wsR + o * q * Ft,
+                                           int64_t(q) * Ft, st->syy[kv], lam, st->wsS + o * Ft, cnt, cs);
+                if (r == cudaSuccess)
+                    r = launch_r2_head(st->wsS + o * Ft, Ft, st->syy[kv], st->nt, c->H, c->d, L,
+                                       st->r2 + (size_t(kv) * c->L_t + st->t0) * c->L_s, c->L_s, cnt, cs);
+                return r;
+            });
         }
         for (int kv = 0; kv < 2 && e == cudaSuccess; ++kv)
             e = launch_topk(st->r2 + (size_t(kv) * c->L_t + st->t0) * c->L_s, st->nt, c->L_s, c->k,
@@ -530,8 +550,13 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
     const int q = c->H * c->d;
     const int64_t p = static_cast<int64_t>(c->k) * q;
     const size_t wes = w_dtype == KVB_F32 ? 4 : 2;
+    // The K and V systems of every target layer go through the factorisation and
+    // the solves together, as many per batch as the workspace budget holds.
+    const int n_sys = 2 * st->nt;
+    const int64_t lp0 = ((p + 63) / 64) * 64 * 64;
+    const int64_t per_sys = 4 * (p * p + p * q + lp0 + p) + static_cast<int64_t>(tc_update_ws_bytes(p, q, 1));
     const int64_t budget = static_cast<int64_t>(ws_budget());
-    int B = static_cast<int>(std::min<int64_t>({MAX_SYS, st->nt, std::max<int64_t>(1, budget / (p * p * 4))}));
+    int B = static_cast<int>(std::min<int64_t>(n_sys, std::max<int64_t>(1, budget / per_sys)));
     if ((s = ws_grow(st, &st->wsG, &st->wsG_bytes, size_t(B) * p * p * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsR, &st->wsR_bytes, size_t(B) * p * q * 4)) != KVB_OK) return s;
     if ((s = ws_grow(st, &st->wsD, &st->wsD_bytes, size_t(B) * p * 4)) != KVB_OK) return s;
@@ -546,30 +571,48 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
     const int32_t* selh[2] = {sel_k_host, sel_v_host};
     {
         ProfScope ps(c, cs, "ridge_solve");
-        for (int kv = 0; kv < 2 && e == cudaSuccess; ++kv) {
-            for (int t0 = st->t0; t0 < t_end && e == cudaSuccess; t0 += B) {
-                const int nb = std::min(B, t_end - t0);
-                SysLayers L;
-                SysOut O;
-                std::memset(&L, 0, sizeof(L));
-                std::memset(&O, 0, sizeof(O));
-                for (int b = 0; b < nb; ++b) {
-                    const int t = t0 + b;
-                    for (int j = 0; j < c->k; ++j) L.layer[b][j] = selh[kv][t * c->k + j];
-                    L.col0[b] = int64_t(t - st->t0) * q;  // column of the block's statistics
-                    O.W[b] = static_cast<char*>(Wout[kv]) + size_t(t) * q * p * wes;
-                    O.bias[b] = bout[kv] + size_t(t) * q;
+        for (int s0 = 0; s0 < n_sys && e == cudaSuccess; s0 += B) {
+            const int nb = std::min(B, n_sys - s0);
+            // the batch's systems of one cache at a time (system i: kv i / nt, target
+            // layer t0 + i % nt), at most MAX_SYS per launch of the per-system kernels
+            auto slices = [&](auto&& fn) {
+                for (int a = 0; a < nb && e == cudaSuccess;) {
+                    const int kv = (s0 + a) / st->nt;
+                    const int end = std::min({nb, (kv + 1) * st->nt - s0, a + MAX_SYS});
+                    SysLayers L;
+                    SysOut O;
+                    std::memset(&L, 0, sizeof(L));
+                    std::memset(&O, 0, sizeof(O));
+                    for (int b = a; b < end; ++b) {
+                        const int t = st->t0 + (s0 + b) % st->nt;
+                        for (int j = 0; j < c->k; ++j) L.layer[b - a][j] = selh[kv][t * c->k + j];
+                        L.col0[b - a] = int64_t(t - st->t0) * q;  // column of the block's statistics
+                        O.W[b - a] = static_cast<char*>(Wout[kv]) + size_t(t) * q * p * wes;
+                        O.bias[b - a] = bout[kv] + size_t(t) * q;
+                    }
+                    e = fn(kv, static_cast<size_t>(a), end - a, L, O);
+                    a = end;
                 }
-                e = launch_gather_system(st->gram[kv], st->Fs, L, q, p, lam, st->wsG, p * p, st->wsD, nb, cs);
-                if (e == cudaSuccess) e = launch_gather_rhs(st->cross[kv], st->Ft, L, q, p, q, st->wsD, st->wsR, p * q, nb, cs);
-                if (e == cudaSuccess)
-                    e = chol_factor_batched(st->wsG, p, p * p, p, nb, st->numeric, st->wsL, lp, &tc, cs);
-                if (e == cudaSuccess)
-                    e = chol_solve_batched(st->wsG, p, p * p, p, st->wsL, lp, st->wsR, q, p * q, q, nb, &tc, cs);
-                if (e == cudaSuccess) e = launch_write_w(w_dtype, st->wsR, p * q, st->wsD, p, q, O, nb, cs);
-                if (e == cudaSuccess)
-                    e = launch_bias(st->wsR, p * q, st->wsD, p, q, L, q, st->mean[kv], st->mean[2 + kv], O, nb, cs);
-            }
+            };
+            slices([&](int kv, size_t o, int cnt, const SysLayers& L, const SysOut&) {
+                cudaError_t r = launch_gather_system(st->gram[kv], st->Fs, L, q, p, lam, st->wsG + o * p * p, p * p,
+                                                     st->wsD + o * p, cnt, cs);
+                if (r == cudaSuccess)
+                    r = launch_gather_rhs(st->cross[kv], st->Ft, L, q, p, q, st->wsD + o * p, st->wsR + o * p * q,
+                                          p * q, cnt, cs);
+                return r;
+            });
+            if (e == cudaSuccess) e = chol_factor_batched(st->wsG, p, p * p, p, nb, st->numeric, st->wsL, lp, &tc, cs);
+            if (e == cudaSuccess)
+                e = chol_solve_batched(st->wsG, p, p * p, p, st->wsL, lp, st->wsR, q, p * q, q, nb, &tc, cs);
+            slices([&](int kv, size_t o, int cnt, const SysLayers& L, const SysOut& O) {
+                cudaError_t r =
+                    launch_write_w(w_dtype, st->wsR + o * p * q, p * q, st->wsD + o * p, p, q, O, cnt, cs);
+                if (r == cudaSuccess)
+                    r = launch_bias(st->wsR + o * p * q, p * q, st->wsD + o * p, p, q, L, q, st->mean[kv],
+                                    st->mean[2 + kv], O, cnt, cs);
+                return r;
+            });
         }
     }
     if (e != cudaSuccess) return cuda_fail(e, "ridge solve");

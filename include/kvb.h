@@ -45,6 +45,12 @@
  * kvb_last_error().  Errors found by the kernels themselves (a bad position,
  * a bounded device wait that gave up) are recorded on the context and returned
  * by kvb_ctx_check() and by the next call on that context.
+ *
+ * Environment: KVB_WAIT_TIMEOUT_MS (default 2000) bounds every device-side
+ * wait, read when a context is created.  KVB_MAP_PAIR=0, KVB_MAP_PAIR_STATIC=1,
+ * KVB_MAP_FUSED_STRIP=0 and KVB_STATS_PAIR=0 select the slower comparison
+ * kernels (single-CTA map, fixed tile-per-pair map, separate strip pass,
+ * single-CTA statistics); results agree with the defaults within rounding.
  */
 #ifndef KVB_H
 #define KVB_H

@@ -12,14 +12,18 @@
 // least 2^-16 of the leading one: x1y1, x1y2, x2y1, x1y3, x2y2, x3y1.  The
 // dropped terms are below 2^-23 of |x||y|, the rounding of an fp32 FMA.
 //
-// One CTA per 128 x 256 output tile (grid N-tiles x M-tiles x batch), two
-// CTAs per SM: warp 0 issues TMA (A and B parts, 3-D maps over [batch][rows]
+// solve_gemm_kernel: one CTA per 128 x 256 output tile (grid N-tiles x
+// M-tiles x batch), two CTAs per SM (solve_gemm_persistent_kernel below is
+// the default): warp 0 issues TMA (A and B parts, 3-D maps over [batch][rows]
 // [64]), warp 1 issues tcgen05.mma kind::f16 (M 128, N 256, K 16) into a
 // 256-column TMEM accumulator, warps 2..5 read it back (through the then idle
 // pipeline shared memory, so that C is updated with coalesced row accesses)
 // and write alpha * acc + beta * C.  With `lower`, tiles wholly above the
 // diagonal are skipped.
 // Every wait is bounded (DevErr::timeout_ns) like the mapper kernel's.
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <string>
 
 #include "kvb_internal.h"
@@ -52,6 +56,8 @@ struct Params {
     int M, N, lower, nkb;  // nkb: 64-wide K blocks (1 to 4)
     float alpha, beta;
     DevErr err;
+    // persistent kernel: tiles per system and in all
+    int nn, tiles_per_sys, total;
 };
 
 struct Maps {
@@ -214,6 +220,218 @@ __global__ void __launch_bounds__(NUM_THREADS, 2) solve_gemm_kernel(const __grid
     }
 }
 
+// Persistent form of the same update: one CTA per SM walks the tiles (system,
+// row block, column block; with `lower`, only tiles touching the lower
+// triangle), four 48 KB stages, the accumulator double buffered in TMEM (2 x
+// 256 columns) so that one tile's read-modify-write of C overlaps the next
+// tile's products.  Epilogue: eight warps, two threads per row (128 columns
+// each), 16 columns per step as two 32-byte (one-sector) accesses, C loaded
+// two steps ahead of the accumulator.  Needs C, ldc and strideC 32-byte aligned.
+constexpr int PSTAGES = 4;
+constexpr int PEPI_WARPS = 8;
+constexpr int PNUM_THREADS = 64 + 32 * PEPI_WARPS;
+constexpr int PSMEM_BYTES = PSTAGES * STAGE_BYTES + 1024 + 256;
+
+__device__ __forceinline__ void decode_tile(const Params& P, int t, int& bz, int& mi, int& nj) {
+    bz = t / P.tiles_per_sys;
+    int r = t - bz * P.tiles_per_sys;
+    if (!P.lower) {
+        mi = r / P.nn;
+        nj = r - mi * P.nn;
+        return;
+    }
+    for (mi = 0;; ++mi) {  // row block mi holds the column blocks nj with nj * BN <= mi * BM + BM - 1
+        const int cnt = min(P.nn, (mi * BM + BM - 1) / BN + 1);
+        if (r < cnt) break;
+        r -= cnt;
+    }
+    nj = r;
+}
+
+__global__ void __launch_bounds__(PNUM_THREADS, 1) solve_gemm_persistent_kernel(const __grid_constant__ Maps Mp,
+                                                                                const __grid_constant__ Params P) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + PSTAGES * A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + PSTAGES * STAGE_BYTES);
+    uint64_t* empty = full + PSTAGES;
+    uint64_t* tfull = empty + PSTAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PSTAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 32 * PEPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 2 * TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int iters = P.nkb * NPROD;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------- producer
+            int issued_phase[PSTAGES];
+            for (int s = 0; s < PSTAGES; ++s) issued_phase[s] = -1;
+            uint32_t phase = 0;
+            int stage = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < P.total; t += gridDim.x) {
+                int bz, mi, nj;
+                decode_tile(P, t, bz, mi, nj);
+                for (int it = 0; it < iters; ++it) {
+                    const int kb = it / NPROD, pr = it - kb * NPROD;
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    tma_load_3d(sA + stage * A_BYTES, &Mp.a[kPartA[pr]], &full[stage], kb * BK, mi * BM, bz);
+                    tma_load_3d(sB + stage * B_BYTES, &Mp.b[kPartB[pr]], &full[stage], kb * BK, nj * BN, bz);
+                    issued_phase[stage] = static_cast<int>(phase);
+                    if (++stage == PSTAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int s = 0; s < PSTAGES; ++s)
+                if (issued_phase[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(issued_phase[s]), DRAIN_NS);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            uint32_t phase = 0;
+            int stage = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < P.total; t += gridDim.x) {
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, P.err, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TMEM_COLS);
+                for (int it = 0; it < iters; ++it) {
+                    if (!mbar_wait(&full[stage], phase, P.err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
+                    const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_bf16(d_tmem, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc,
+                                  (it | k) != 0);
+                    umma_commit(&empty[stage]);
+                    if (++stage == PSTAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            umma_commit(drain);  // every MMA issued here completes before TMEM is released
+            mbar_wait_drain(drain, 0, DRAIN_NS);
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int sub = warp & 3;              // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;      // columns [0,128) or [128,256) of the tile
+        const int row = sub * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < P.total; t += gridDim.x) {
+            int bz, mi, nj;
+            decode_tile(P, t, bz, mi, nj);
+            const int r = mi * BM + row;
+            const int n0 = nj * BN + 128 * half;
+            const int ncol = max(0, min(128, P.N - n0));  // multiple of 16
+            const bool live = r < P.M;
+            const bool rd = live && P.beta != 0.f;
+            float* crow = P.C + bz * P.strideC + static_cast<int64_t>(r) * P.ldc + n0;
+            // C two steps ahead: cur = step c0, nxt = step c0 + 16
+            uint32_t cur[2][8] = {}, nxt[2][8] = {};
+            if (rd && ncol > 0) {
+                ld_global_v8(crow, cur[0]);
+                ld_global_v8(crow + 8, cur[1]);
+            }
+            if (rd && ncol > 16) {
+                ld_global_v8(crow + 16, nxt[0]);
+                ld_global_v8(crow + 24, nxt[1]);
+            }
+            if (!mbar_wait(&tfull[acc], acc_phase, P.err, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) +
+                                   static_cast<uint32_t>(acc * TMEM_COLS + 128 * half);
+#pragma unroll 1
+            for (int c0 = 0; c0 < ncol; c0 += 16) {
+                uint32_t nn2[2][8] = {};
+                if (rd && c0 + 32 < ncol) {
+                    ld_global_v8(crow + c0 + 32, nn2[0]);
+                    ld_global_v8(crow + c0 + 40, nn2[1]);
+                }
+                uint32_t v[16];
+                tmem_ld16(tbase + c0, v);
+                tmem_ld_wait();
+                if (live) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            o[e] = __float_as_uint(
+                                fmaf(P.beta, __uint_as_float(cur[h][e]), P.alpha * __uint_as_float(v[8 * h + e])));
+                        st_global_v8(crow + c0 + 8 * h, o);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        cur[h][e] = nxt[h][e];
+                        nxt[h][e] = nn2[h][e];
+                    }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 2 * TMEM_COLS);
+    }
+}
+
 // Three bf16 parts of a rows x K fp32 operand (K <= kp), written K-major as
 // [batch][rows][kp] with zeros beyond K.  Element (r, k) of batch item b is
 // src[b * s_batch + r * s_row + k * s_k]; 32 x 32 tiles through shared
@@ -335,10 +553,31 @@ cudaError_t launch_tc_update(const TcSolve& tc, const TcOperand& A, const TcOper
     P.alpha = alpha;
     P.beta = beta;
     P.err = tc.err;
+    // the persistent kernel's 32-byte accesses need C, ldc and strideC 32-byte aligned
+    const char* env = std::getenv("KVB_SOLVE_PERSIST");
+    const bool persist = !(env && std::strcmp(env, "0") == 0) && (reinterpret_cast<uintptr_t>(C) & 31u) == 0 &&
+                         ldc % 8 == 0 && strideC % 8 == 0;
+    const int nm = static_cast<int>((A.rows + BM - 1) / BM), nn = static_cast<int>((N + BN - 1) / BN);
+    if (persist) {
+        int64_t per_sys = 0;
+        for (int mi = 0; mi < nm; ++mi)
+            per_sys += lower ? std::min<int64_t>(nn, (int64_t(mi) * BM + BM - 1) / BN + 1) : nn;
+        const int64_t total = per_sys * batch;
+        if (total > 0 && total <= 0x7fffffffLL) {
+            P.nn = nn;
+            P.tiles_per_sys = static_cast<int>(per_sys);
+            P.total = static_cast<int>(total);
+            e = cudaFuncSetAttribute(solve_gemm_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     PSMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            const int grid = static_cast<int>(total < tc.num_sms ? total : tc.num_sms);
+            solve_gemm_persistent_kernel<<<grid, PNUM_THREADS, PSMEM_BYTES, s>>>(mp, P);
+            return cudaGetLastError();
+        }
+    }
     e = cudaFuncSetAttribute(solve_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((A.rows + BM - 1) / BM),
-              static_cast<unsigned>(batch));
+    dim3 grid(static_cast<unsigned>(nn), static_cast<unsigned>(nm), static_cast<unsigned>(batch));
     solve_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(mp, P);
     return cudaGetLastError();
 }

@@ -181,6 +181,23 @@ def test_statistics_on_cta_pairs_and_single_ctas_agree(kvb, monkeypatch):
             assert rel_fro(x, y) <= 1e-6
 
 
+def test_persistent_and_per_tile_solver_updates_agree(kvb, monkeypatch):
+    # 1024-wide systems with 768 right-hand sides: the tensor-core updates run on the
+    # persistent kernel by default and on the per-tile kernel with KVB_SOLVE_PERSIST=0
+    pair = round_pair(make_pair(13, 4, 3, 2, 128, 2, 1024, 6, 1e4, 1e6, noise=1e-2, sigma=1.0), torch.bfloat16)
+    ctx = _ctx(kvb, pair, 1024)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, 1024)
+    _accumulate(kvb, ctx, st, pair["calib"], torch.bfloat16)
+    a = _run_fit(kvb, ctx, st, pair, torch.float32)
+    monkeypatch.setenv("KVB_SOLVE_PERSIST", "0")
+    b = _run_fit(kvb, ctx, st, pair, torch.float32)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert np.abs(a[2] - b[2]).max() <= 1e-5
+    for x, y in zip(a[3:], b[3:]):
+        assert rel_fro(to_host64(x), to_host64(y)) <= 1e-5
+    _check_fit(kvb, ctx, st, pair, torch.float32, TOL_W)
+
+
 @pytest.mark.parametrize("d,H", [(32, 8), (64, 4), (16, 16)])
 def test_bf16_tensor_core_statistics_head_dims_packed_short_sequences(kvb, d, H):
     # H*d = 256, so the statistics run on the tensor cores; the single-pass gather

@@ -118,6 +118,18 @@ def test_fp32_fit_system_size_not_a_multiple_of_the_panels(kvb):
     _check_fit(kvb, ctx, st, pair, torch.float32, 1e-4)
 
 
+def test_fp32_fit_ragged_tensor_core_updates(kvb):
+    # head_dim 64, 5 KV heads, k = 3: ridge systems of 960 unknowns whose trailing
+    # updates (704 and 448 rows and columns) and right-hand-side updates (320 columns)
+    # run on the tensor cores with partial 128 x 256 tiles in both directions
+    pair = make_pair(6, 4, 3, 5, 64, 3, 512, 8, 1e4, 1e6)
+    ctx = _ctx(kvb, pair, 512)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 512)
+    _accumulate(kvb, ctx, st, pair["calib"], torch.float32)
+    assert kvb.kvb_stats_count(st) == 1024
+    _check_fit(kvb, ctx, st, pair, torch.float32, 1e-4)
+
+
 def test_chan_merge_over_ragged_batches_and_offsets(kvb):
     # unequal batch lengths, positions not starting at 0: merges must equal two-pass statistics
     rng = np.random.default_rng(3)

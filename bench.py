@@ -557,9 +557,9 @@ def run_gpu(args, rank, world, local_rank):
 
     # ---------------- end to end: pinned host buffers, copies inside the timed region.
     # Every step copies its source cache and positions host -> device, maps, and copies the
-    # mapped cache device -> host.  Steps are pipelined: device buffers are double-buffered
-    # and the copy-in of step i+1 / copy-out of step i-1 run on their own streams while
-    # step i maps.
+    # mapped cache device -> host.  Steps are pipelined over args.e2e_buffers device buffer
+    # sets: the copy-in of later steps and the copy-out of earlier ones run on their own
+    # streams while step i maps.
     h_src_k = torch.empty(src_k.shape, dtype=src_k.dtype, pin_memory=True)
     h_src_v = torch.empty(src_v.shape, dtype=src_v.dtype, pin_memory=True)
     h_pos = torch.empty(pos.shape, dtype=pos.dtype, pin_memory=True)
@@ -570,17 +570,18 @@ def run_gpu(args, rank, world, local_rank):
     h_pos.copy_(pos)
     h2d = h_src_k.numel() * 2 + h_src_v.numel() * 2 + h_pos.numel() * 4
     d2h = h_out_k.numel() * 2 + h_out_v.numel() * 2
-    bufs = [(src_k, src_v, pos, out_k, out_v),
-            (torch.empty_like(src_k), torch.empty_like(src_v), torch.empty_like(pos), torch.empty_like(out_k),
-             torch.empty_like(out_v))]
+    nbuf = max(2, args.e2e_buffers)
+    bufs = [(src_k, src_v, pos, out_k, out_v)] + [
+        (torch.empty_like(src_k), torch.empty_like(src_v), torch.empty_like(pos), torch.empty_like(out_k),
+         torch.empty_like(out_v)) for _ in range(nbuf - 1)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def run_e2e(n_steps, start_event):
         s_in.wait_event(start_event)
         s_out.wait_event(start_event)
-        ev_comp, ev_out = [None, None], [None, None]
+        ev_comp, ev_out = [None] * nbuf, [None] * nbuf
         for i in range(n_steps):
-            b = i % 2
+            b = i % nbuf
             sk, sv, ps, ok, ov = bufs[b]
             with torch.cuda.stream(s_in):
                 if ev_comp[b] is not None:  # the map that last read this buffer is done
@@ -695,8 +696,8 @@ def run_gpu(args, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
                 "how": "kvb_map_apply on device copies of pinned host caches; per step H2D of source K/V + "
-                       "positions and D2H of target K/V; steps pipelined on copy/compute streams with "
-                       "double-buffered device buffers"},
+                       "positions and D2H of target K/V; steps pipelined on copy/compute streams over "
+                       f"{nbuf} device buffer sets"},
         "fit": fit,
         "attention_cosine": attn_roofline(attn, clk),
         "fp32_map": fp32_map,
@@ -722,6 +723,8 @@ def main():
     ap.add_argument("--skip-fp32", action="store_true", help="skip the fp32-cache map leg")
     ap.add_argument("--fp32-only", action="store_true", help="run only the fp32-cache map leg")
     ap.add_argument("--fit-only", action="store_true", help="run only the fit leg (with --workload small: 8 -> 8 layers)")
+    ap.add_argument("--e2e-buffers", type=int, default=2,
+                    help="device buffer sets the end-to-end leg pipelines its steps over")
     ap.add_argument("--fit-block", type=int, default=0,
                     help="fit leg with statistics of this many target layers at a time (one pass per block)")
     args = ap.parse_args()

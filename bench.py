@@ -204,7 +204,7 @@ FIT = dict(L_s=40, L_t=64, H=8, d=128, k=8, seq_len=1024, n_seq=256, batch_token
 FIT_SMALL = dict(FIT, L_s=8, L_t=8, k=4, n_seq=32)
 
 
-def run_fit(kvb, dev, seed=101, small=False, block=0):
+def run_fit(kvb, dev, seed=101, small=False, block=0, f32=False):
     """Calibration statistics + selection + ridge solve, Qwen3-14B->32B shapes.
 
     256 sequences x 1024 tokens (positions 0..1023) streamed in 32 batches of
@@ -213,8 +213,9 @@ def run_fit(kvb, dev, seed=101, small=False, block=0):
     hidden top-8 affine map (applied with kvb_map_apply) plus noise at SNR 10;
     every batch distinct, generated between the timed accumulate calls.  With
     block > 0 the statistics hold `block` target layers at a time (bounded
-    memory) and every block re-streams the 32 batches.  Returns a dict for the
-    JSON line.
+    memory) and every block re-streams the 32 batches.  With f32 the caches are
+    handed over as fp32 (their bf16 values widened outside the timed region).
+    Returns a dict for the JSON line.
     """
     import torch
     import synth
@@ -269,12 +270,13 @@ def run_fit(kvb, dev, seed=101, small=False, block=0):
             kern[n] = (c0 + c, t0_ + t)
 
     for t_begin, t_end in blocks:
-        st = kvb.kvb_stats_create_block(ctx, kvb.KVB_BF16, Tb, t_begin, t_end)
+        st = kvb.kvb_stats_create_block(ctx, kvb.KVB_F32 if f32 else kvb.KVB_BF16, Tb, t_begin, t_end)
         for b in range(n_batches):  # every batch distinct; only the accumulate calls are timed
             make_batch(b)
+            caches = [x.float() for x in (sk, sv, tk, tv)] if f32 else (sk, sv, tk, tv)
             kvb.kvb_profile_enable(ctx, True)
             e0.record(stream)
-            kvb.kvb_stats_accumulate(ctx, st, sk, sv, tk, tv, pos, F["stride"], stream)
+            kvb.kvb_stats_accumulate(ctx, st, *caches, pos, F["stride"], stream)
             e1.record(stream)
             kvb.kvb_profile_enable(ctx, False)
             torch.cuda.synchronize(dev)
@@ -306,13 +308,15 @@ def run_fit(kvb, dev, seed=101, small=False, block=0):
     blk = max(t1 - t0 for t0, t1 in blocks)
     out = {"workload": (f"{L_s}->{L_t} layers, k={k}, " if small else "qwen3-14b->32b-shaped fit: ") +
                        f"{F['n_seq']} x {F['seq_len']} calibration tokens in {n_batches} batches of {Tb}, stride 4, "
-                       "bf16 caches, fp32 statistics (split-bf16 tensor-core products), lambda 0.01",
+                       + ("fp32 caches, fp32 statistics (three-part bf16 tensor-core products), lambda 0.01" if f32 else
+                          "bf16 caches, fp32 statistics (split-bf16 tensor-core products), lambda 0.01"),
            "n_obs": n_obs, "batches": n_batches, "target_block": blk, "passes": len(blocks),
            "stats_bytes": 2 * 4 * (Fs * Fs + Fs * blk * q),
            "stats_ms": stats_ms, "stats_gemm_kernel": gemm_name, "stats_gemm_ms": gemm_ms,
            "stats_gemm_tflops_algorithmic": flop_alg / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
-           "stats_gemm_tflops_executed": 3 * flop_alg / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
-           "gather_ms": gather_ms, "gather_gbs": gather_bytes / (gather_ms / 1e3) / 1e9 if gather_ms else None,
+           "stats_gemm_tflops_executed": (6 if f32 else 3) * flop_alg / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
+           "gather_ms": gather_ms,
+           "gather_gbs": gather_bytes / (gather_ms / 1e3) / 1e9 if gather_ms and not f32 else None,  # bf16 single pass
            "select_s": t_sel, "ridge_s": t_ridge,
            "selection_recovered": float((np.asarray(gk) == sel_k).mean() + (np.asarray(gv) == sel_v).mean()) / 2,
            "kernels": {n: {"launches": c, "total_ms": t} for n, (c, t) in kern.items()}}
@@ -723,6 +727,7 @@ def main():
     ap.add_argument("--skip-fp32", action="store_true", help="skip the fp32-cache map leg")
     ap.add_argument("--fp32-only", action="store_true", help="run only the fp32-cache map leg")
     ap.add_argument("--fit-only", action="store_true", help="run only the fit leg (with --workload small: 8 -> 8 layers)")
+    ap.add_argument("--fit-f32", action="store_true", help="fit leg with fp32 caches (with --fit-only)")
     ap.add_argument("--e2e-buffers", type=int, default=2,
                     help="device buffer sets the end-to-end leg pipelines its steps over")
     ap.add_argument("--fit-block", type=int, default=0,
@@ -750,7 +755,7 @@ def main():
         elif args.fp32_only:
             res = {"fp32_map": run_fp32_map(kvb, dev)}
         else:
-            res = {"fit": run_fit(kvb, dev, small=args.workload == "small", block=args.fit_block)}
+            res = {"fit": run_fit(kvb, dev, small=args.workload == "small", block=args.fit_block, f32=args.fit_f32)}
         if rank == 0:
             print(json.dumps(res), flush=True)
         return

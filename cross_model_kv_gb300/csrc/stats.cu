@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(256) center_transpose_kernel(const T* __restri
                                                                const float2* __restrict__ tab, bool strip,
                                                                const float* __restrict__ mean,
                                                                void* __restrict__ out, void* __restrict__ out_lo,
-                                                               int64_t ld) {
+                                                               void* __restrict__ out_3, int64_t ld) {
     extern __shared__ float tile[];  // [64][d + 1]
     const int slab = blockIdx.x;
     const int r0 = blockIdx.y * 64;
@@ -168,10 +168,17 @@ __global__ void __launch_bounds__(256) center_transpose_kernel(const T* __restri
         const float v = tile[rr * ldt + e];
         if (out_lo == nullptr) {
             static_cast<float*>(out)[o] = v;
-        } else {
+        } else if (out_3 == nullptr) {
             const __nv_bfloat16 hi = __float2bfloat16_rn(v);
             static_cast<__nv_bfloat16*>(out)[o] = hi;
             static_cast<__nv_bfloat16*>(out_lo)[o] = __float2bfloat16_rn(v - __bfloat162float(hi));
+        } else {  // three parts: x1 = bf16(v), x2 = bf16(v - x1), x3 = bf16(v - x1 - x2)
+            const __nv_bfloat16 x1 = __float2bfloat16_rn(v);
+            const float e1 = v - __bfloat162float(x1);
+            const __nv_bfloat16 x2 = __float2bfloat16_rn(e1);
+            static_cast<__nv_bfloat16*>(out)[o] = x1;
+            static_cast<__nv_bfloat16*>(out_lo)[o] = x2;
+            static_cast<__nv_bfloat16*>(out_3)[o] = __float2bfloat16_rn(e1 - __bfloat162float(x2));
         }
     }
 }
@@ -636,7 +643,8 @@ __global__ void chan_finish_kernel(long long* __restrict__ n_dev, const int* __r
 
 // S_yy[j] += sum_r Z[j][r]^2 - g zbar_j^2 + f delta_j^2.  One warp per column.
 // Z is float32, or a (hi, lo) bf16 pair when lo != nullptr.
-__global__ void syy_kernel(const void* __restrict__ Y, const void* __restrict__ Ylo, int64_t ld, int64_t rows_n,
+__global__ void syy_kernel(const void* __restrict__ Y, const void* __restrict__ Ylo, const void* __restrict__ Y3,
+                           int64_t ld, int64_t rows_n,
                            const int* __restrict__ nb, const float* __restrict__ dy, const float* __restrict__ zy,
                            const float* __restrict__ coef, float* __restrict__ syy) {
     const int64_t j = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
@@ -650,7 +658,8 @@ __global__ void syy_kernel(const void* __restrict__ Y, const void* __restrict__ 
             v = static_cast<const float*>(Y)[j * ld + r];
         else
             v = __bfloat162float(static_cast<const __nv_bfloat16*>(Y)[j * ld + r]) +
-                __bfloat162float(static_cast<const __nv_bfloat16*>(Ylo)[j * ld + r]);
+                __bfloat162float(static_cast<const __nv_bfloat16*>(Ylo)[j * ld + r]) +
+                (Y3 ? __bfloat162float(static_cast<const __nv_bfloat16*>(Y3)[j * ld + r]) : 0.f);
         s = fmaf(v, v, s);
     }
 #pragma unroll
@@ -807,13 +816,13 @@ cudaError_t launch_gather(const GatherArgs& g, cudaStream_t s) {
         cudaFuncSetAttribute(center_transpose_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 80 * 1024);
         center_transpose_kernel<float><<<grid, 256, smem, s>>>(static_cast<const float*>(g.cache), g.T, g.d, g.rows,
                                                                g.nb, g.pos, g.tab, g.strip, g.bmean, g.out, g.out_lo,
-                                                               g.ld);
+                                                               g.out_3, g.ld);
     } else {
         cudaFuncSetAttribute(center_transpose_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              80 * 1024);
         center_transpose_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(
             static_cast<const __nv_bfloat16*>(g.cache), g.T, g.d, g.rows, g.nb, g.pos, g.tab, g.strip, g.bmean, g.out,
-            g.out_lo, g.ld);
+            g.out_lo, g.out_3, g.ld);
     }
     return cudaGetLastError();
 }
@@ -829,12 +838,12 @@ cudaError_t launch_chan_finish(long long* n_dev, const int* nb, cudaStream_t s) 
     return cudaGetLastError();
 }
 
-cudaError_t launch_syy(const void* Y, const void* Ylo, int64_t ld, int64_t rows_n, const int* nb, const float* dy,
+cudaError_t launch_syy(const void* Y, const void* Ylo, const void* Y3, int64_t ld, int64_t rows_n, const int* nb, const float* dy,
                        const float* zy, const float* coef, float* syy, cudaStream_t s) {
     const int64_t threads = rows_n * 32;
     const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
     if (blocks == 0) return cudaSuccess;
-    syy_kernel<<<blocks, 256, 0, s>>>(Y, Ylo, ld, rows_n, nb, dy, zy, coef, syy);
+    syy_kernel<<<blocks, 256, 0, s>>>(Y, Ylo, Y3, ld, rows_n, nb, dy, zy, coef, syy);
     return cudaGetLastError();
 }
 

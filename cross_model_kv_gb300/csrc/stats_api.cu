@@ -6,6 +6,8 @@
 // the statistics of a selection are sub-blocks (centering commutes with
 // choosing columns).
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <cstring>
 #include <vector>
 
@@ -38,6 +40,8 @@ struct kvb_stats {
     void* YT[2] = {};      // centered batch, [Ft][ld]: float32, or bf16 hi part
     void* XT_lo[2] = {};   // bf16 lo parts (tensor-core path only)
     void* YT_lo[2] = {};
+    void* XT_3[2] = {};    // third bf16 parts (tensor-core path, fp32 caches)
+    void* YT_3[2] = {};
     StatsGemmPlan* plan = nullptr;
     bool use_tc = false;
     // fit workspace, allocated on first use
@@ -126,6 +130,8 @@ void stats_jobs(const kvb_stats* st, StatsJob jobs[4]) {
         g.B = st->XT[kv];
         g.A_lo = st->XT_lo[kv];
         g.B_lo = st->XT_lo[kv];
+        g.A_3 = st->XT_3[kv];
+        g.B_3 = st->XT_3[kv];
         g.out = st->gram[kv];
         g.da = st->delta[kv];
         g.db = st->delta[kv];
@@ -140,6 +146,8 @@ void stats_jobs(const kvb_stats* st, StatsJob jobs[4]) {
         x.B = st->YT[kv];
         x.A_lo = st->XT_lo[kv];
         x.B_lo = st->YT_lo[kv];
+        x.A_3 = st->XT_3[kv];
+        x.B_3 = st->YT_3[kv];
         x.out = st->cross[kv];
         x.da = st->delta[kv];
         x.db = st->delta[2 + kv];
@@ -222,8 +230,11 @@ kvb_status kvb_stats_create_block(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_bat
         A(reinterpret_cast<void**>(&st->cross[kv]), static_cast<size_t>(st->Fs) * st->Ft * 4);
         A(reinterpret_cast<void**>(&st->syy[kv]), st->Ft * 4);
     }
-    // Tensor-core statistics for bf16 caches whose shapes tile by 128 x 256.
-    if (s == KVB_OK && dtype == KVB_BF16) {
+    // Tensor-core statistics when the shapes tile by 128 x 256: bf16 caches as two
+    // bf16 parts, fp32 caches as three (unless KVB_STATS_TC_F32=0)
+    const char* f32tc = std::getenv("KVB_STATS_TC_F32");
+    const bool three = dtype == KVB_F32;
+    if (s == KVB_OK && (dtype == KVB_BF16 || !(f32tc && std::strcmp(f32tc, "0") == 0))) {
         StatsJob jobs[4];
         stats_jobs(st, jobs);
         st->use_tc = stats_gemm_tc_supported(jobs, 4);
@@ -234,6 +245,10 @@ kvb_status kvb_stats_create_block(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_bat
             A(&st->XT_lo[kv], static_cast<size_t>(st->Fs) * st->ld * 2);
             A(&st->YT[kv], static_cast<size_t>(st->Ft) * st->ld * 2);
             A(&st->YT_lo[kv], static_cast<size_t>(st->Ft) * st->ld * 2);
+            if (three) {
+                A(&st->XT_3[kv], static_cast<size_t>(st->Fs) * st->ld * 2);
+                A(&st->YT_3[kv], static_cast<size_t>(st->Ft) * st->ld * 2);
+            }
         } else {
             A(&st->XT[kv], static_cast<size_t>(st->Fs) * st->ld * 4);
             A(&st->YT[kv], static_cast<size_t>(st->Ft) * st->ld * 4);
@@ -303,6 +318,7 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
     const float2* tabs[4] = {c->tab_s, nullptr, c->tab_t, nullptr};
     void* outs[4] = {st->XT[0], st->XT[1], st->YT[0], st->YT[1]};
     void* outs_lo[4] = {st->XT_lo[0], st->XT_lo[1], st->YT_lo[0], st->YT_lo[1]};
+    void* outs_3[4] = {st->XT_3[0], st->XT_3[1], st->YT_3[0], st->YT_3[1]};
     cudaError_t e;
     {
         ProfScope ps(c, cs, "calib_select_rows");
@@ -334,6 +350,7 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
             g.bmean = st->bmean[m];
             g.out = outs[m];
             g.out_lo = outs_lo[m];
+            g.out_3 = outs_3[m];
             g.ld = st->ld;
             e = launch_gather(g, cs);
         }
@@ -369,7 +386,7 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
     {
         ProfScope ps(c, cs, "calib_syy_merge");
         for (int kv = 0; kv < 2 && e == cudaSuccess; ++kv)
-            e = launch_syy(st->YT[kv], st->YT_lo[kv], st->ld, st->Ft, st->nb_dev, st->delta[2 + kv], st->zbar[2 + kv],
+            e = launch_syy(st->YT[kv], st->YT_lo[kv], st->YT_3[kv], st->ld, st->Ft, st->nb_dev, st->delta[2 + kv], st->zbar[2 + kv],
                            st->coef_dev, st->syy[kv], cs);
         if (e == cudaSuccess) e = launch_chan_finish(st->n_dev, st->nb_dev, cs);
     }

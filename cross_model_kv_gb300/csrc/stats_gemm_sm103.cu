@@ -78,12 +78,24 @@ struct Params {
     const int* nb;
     const float* coef;  // {f, g}
     DevErr err;
+    int nprod;  // 3 (operands as two bf16 parts) or 6 (three parts)
     JobP job[4];
 };
 
 struct Maps {
-    CUtensorMap a_hi[4], a_lo[4], b_hi[4], b_lo[4];
+    CUtensorMap a_hi[4], a_lo[4], a_3[4], b_hi[4], b_lo[4], b_3[4];
 };
+
+// Operand parts of product `seg`, largest first: two-part operands take
+// hi.hi, hi.lo, lo.hi; three-part operands add hi.3, lo.lo, 3.hi (every product
+// down to 2^-16 of the leading one).
+__device__ __forceinline__ void product_maps(const Maps& M, int job, int seg, const CUtensorMap*& ma,
+                                             const CUtensorMap*& mb) {
+    constexpr int pa[6] = {0, 0, 1, 0, 1, 2}, pb[6] = {0, 1, 0, 2, 1, 0};
+    const int a = pa[seg], b = pb[seg];
+    ma = a == 0 ? &M.a_hi[job] : a == 1 ? &M.a_lo[job] : &M.a_3[job];
+    mb = b == 0 ? &M.b_hi[job] : b == 1 ? &M.b_lo[job] : &M.b_3[job];
+}
 
 __device__ __forceinline__ void decode(uint32_t e, int& job, int& bi, int& bj) {
     job = static_cast<int>(e >> 30);
@@ -185,7 +197,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int nk = (*P.nb + BK - 1) / BK;  // K-blocks per pass (zero padding beyond n_b)
-    const int iters = 3 * nk;
+    const int iters = P.nprod * nk;
 
     if (warp == 0) {
         if (lane == 0 && iters > 0) {
@@ -204,8 +216,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const int seg = it / nk;
                     const int kb = it - seg * nk;
-                    const CUtensorMap* ma = seg == 2 ? &M.a_lo[job] : &M.a_hi[job];
-                    const CUtensorMap* mb = seg == 1 ? &M.b_lo[job] : &M.b_hi[job];
+                    const CUtensorMap *ma, *mb;
+                    product_maps(M, job, seg, ma, mb);
                     mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
                     tma_load_2d(sA + stage * A_BYTES, ma, &full[stage], kb * BK, bi * BM);
                     tma_load_2d(sB + stage * B_BYTES, mb, &full[stage], kb * BK, bj * BN);
@@ -355,7 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int nk = (*P.nb + BK - 1) / BK;  // K-blocks per pass (zero padding beyond n_b)
-    const int iters = 3 * nk;
+    const int iters = P.nprod * nk;
     // a consumer's release of a ring slot, on rank 0's sempty
     auto release_slot = [&](int slot) { mbar_arrive_cluster(mapa_shared(smem_u32(&sempty[slot]), 0)); };
     int slot = 0;
@@ -411,8 +423,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const int seg = it / nk;
                     const int kb = it - seg * nk;
-                    const CUtensorMap* ma = seg == 2 ? &M.a_lo[job] : &M.a_hi[job];
-                    const CUtensorMap* mb = seg == 1 ? &M.b_lo[job] : &M.b_hi[job];
+                    const CUtensorMap *ma, *mb;
+                    product_maps(M, job, seg, ma, mb);
                     const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * PSTAGE_BYTES);
                     tma_load_2d_pair(sA + stage * PA_BYTES, ma, full_leader, kb * BK, bi * PM + 128 * rank);
@@ -597,8 +609,12 @@ cudaError_t launch_stats_gemm_tc(StatsGemmPlan* plan, const StatsJob* jobs, int 
     P.nb = nb;
     P.coef = coef;
     P.err = err;
+    P.nprod = jobs[0].A_3 ? 6 : 3;
     for (int j = 0; j < n_jobs; ++j) {
         const StatsJob& J = jobs[j];
+        if (J.A_3 && (!encode_2d(&M.a_3[j], J.A_3, ld, J.Ma, BM, why) ||
+                      !encode_2d(&M.b_3[j], J.B_3, ld, J.Nb, pair ? 128 : BN, why)))
+            return cudaErrorInvalidValue;
         if (!encode_2d(&M.a_hi[j], J.A, ld, J.Ma, BM, why) || !encode_2d(&M.a_lo[j], J.A_lo, ld, J.Ma, BM, why) ||
             !encode_2d(&M.b_hi[j], J.B, ld, J.Nb, pair ? 128 : BN, why) ||
             !encode_2d(&M.b_lo[j], J.B_lo, ld, J.Nb, pair ? 128 : BN, why))

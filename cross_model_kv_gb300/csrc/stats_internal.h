@@ -41,6 +41,7 @@ struct GatherArgs {
     float* bmean;             // [n_slabs*d] batch mean (generic path)
     void* out;
     void* out_lo;
+    void* out_3;              // third bf16 part (fp32 caches on the tensor-core path), or NULL
     int64_t ld;
 };
 bool gather_single_pass_ok(kvb_dtype dt, int d);
@@ -53,7 +54,7 @@ cudaError_t launch_chan_prepare(const MeanSet& ms, const long long* n_dev, const
                                 cudaStream_t s);
 cudaError_t launch_symmetrize(const float* src, float* dst, int64_t n, cudaStream_t s);
 cudaError_t launch_chan_finish(long long* n_dev, const int* nb, cudaStream_t s);
-cudaError_t launch_syy(const void* Y, const void* Ylo, int64_t ld, int64_t rows_n, const int* nb, const float* dy,
+cudaError_t launch_syy(const void* Y, const void* Ylo, const void* Y3, int64_t ld, int64_t rows_n, const int* nb, const float* dy,
                        const float* zy, const float* coef, float* syy, cudaStream_t s);
 cudaError_t launch_stats_gemm_simt(const float* A, const float* B, int64_t ld, int64_t Ma, int64_t Nb, bool lower,
                                    const float* da, const float* db, const float* za, const float* zb,
@@ -61,14 +62,18 @@ cudaError_t launch_stats_gemm_simt(const float* A, const float* B, int64_t ld, i
 
 // Statistics GEMM jobs, K = observations:
 //   out[i][j] += sum_r A[i][r] B[j][r] - g za[i] zb[j] + f da[i] db[j].
-// CUDA-core path: A, B float32 [rows][ld].  Tensor-core path: A = A + A_lo and
-// B = B + B_lo as bf16 pairs; the product is taken as A.B + A.B_lo + A_lo.B
-// (three bf16 passes into one fp32 accumulator; A_lo.B_lo is below fp32 noise).
+// CUDA-core path: A, B float32 [rows][ld].  Tensor-core path, bf16 caches: A =
+// A + A_lo and B = B + B_lo as bf16 pairs; the product is taken as A.B + A.B_lo
+// + A_lo.B (three bf16 passes into one fp32 accumulator; A_lo.B_lo is below fp32
+// noise).  Tensor-core path, fp32 caches: three parts A + A_lo + A_3 (24
+// significant bits) and the six products down to 2^-16 of the leading one.
 struct StatsJob {
     const void* A;   // [Ma][ld]
     const void* B;   // [Nb][ld]
     const void* A_lo;
     const void* B_lo;
+    const void* A_3;  // third parts, or NULL (two-part operands)
+    const void* B_3;
     float* out;      // [Ma][ldo]
     const float* da;
     const float* db;

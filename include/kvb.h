@@ -48,10 +48,11 @@
  *
  * Environment: KVB_WAIT_TIMEOUT_MS (default 2000) bounds every device-side
  * wait, read when a context is created.  KVB_MAP_PAIR=0, KVB_MAP_PAIR_STATIC=1,
- * KVB_MAP_FUSED_STRIP=0, KVB_STATS_PAIR=0 and KVB_SOLVE_PERSIST=0 select the
- * slower comparison kernels (single-CTA map, fixed tile-per-pair map, separate
- * strip pass, single-CTA statistics, per-tile solver updates); results agree
- * with the defaults within rounding.
+ * KVB_MAP_FUSED_STRIP=0, KVB_STATS_PAIR=0, KVB_SOLVE_PERSIST=0 and
+ * KVB_STATS_TC_F32=0 select the slower comparison kernels (single-CTA map,
+ * fixed tile-per-pair map, separate strip pass, single-CTA statistics,
+ * per-tile solver updates, CUDA-core statistics for fp32 caches); results
+ * agree with the defaults within rounding.
  */
 #ifndef KVB_H
 #define KVB_H

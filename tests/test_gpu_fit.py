@@ -193,6 +193,33 @@ def test_statistics_on_cta_pairs_and_single_ctas_agree(kvb, monkeypatch):
             assert rel_fro(x, y) <= 1e-6
 
 
+def test_fp32_statistics_on_tensor_cores_match_cuda_cores(kvb, monkeypatch):
+    # fp32 caches whose shapes tile (1024 source x 768 target features): the statistics
+    # run on the tensor cores with three bf16 parts per operand (six products), and on
+    # the CUDA cores with KVB_STATS_TC_F32=0; both are fp32-accurate
+    pair = make_pair(14, 4, 3, 2, 128, 2, 512, 8, 1e4, 1e6, noise=1e-2, sigma=1.0)
+    ctx = _ctx(kvb, pair, 512)
+    kvb.kvb_profile_enable(ctx, True)
+    st_tc = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 512)
+    _accumulate(kvb, ctx, st_tc, pair["calib"], torch.float32)
+    assert "stats_gemm_tcgen05" in kvb.kvb_profile_read(ctx)
+    monkeypatch.setenv("KVB_STATS_TC_F32", "0")
+    st_cc = kvb.kvb_stats_create(ctx, kvb.KVB_F32, 512)
+    monkeypatch.delenv("KVB_STATS_TC_F32")
+    _accumulate(kvb, ctx, st_cc, pair["calib"], torch.float32)
+    assert "stats_gemm_simt" in kvb.kvb_profile_read(ctx)
+    _check_stats(kvb, st_tc, pair, 1e-5)
+    q = pair["H"] * pair["d"]
+    for kv in (0, 1):
+        a = _export(kvb, st_tc, kv, pair["L_s"] * q, pair["L_t"] * q)
+        b = _export(kvb, st_cc, kv, pair["L_s"] * q, pair["L_t"] * q)
+        # both sum ~1024 fp32 products per entry and batch in different orders: each is
+        # within ~sqrt(1024) * 2^-24 ~ 2e-6 of the exact sums, as the oracle checks bound
+        for x, y in zip(a[1:], b[1:]):
+            assert rel_fro(x, y) <= 1e-5
+    _check_fit(kvb, ctx, st_tc, pair, torch.float32, 1e-4)
+
+
 def test_persistent_and_per_tile_solver_updates_agree(kvb, monkeypatch):
     # 1024-wide systems with 768 right-hand sides: the tensor-core updates run on the
     # persistent kernel by default and on the per-tile kernel with KVB_SOLVE_PERSIST=0

@@ -123,6 +123,22 @@ def test_tensor_core_unsorted_positions_partial_row_blocks(kvb):
     assert np.all(got[:, :, q_pos < 0] == 0)
 
 
+def test_tensor_core_rising_maxima_over_many_key_tiles(kvb):
+    # tensor-core kernel against the oracle: row maxima that rise by more than 2^8
+    # (base 2) several times across 9 key tiles, so that O is rescaled in TMEM, a
+    # ragged last tile, a partial row block, and causal suffix queries that see 1 to
+    # 9 tiles
+    T = 1100
+    q_pos = np.concatenate([np.arange(T - 70, T), [0, 1, 127, 128, 129, 500]])
+    c = Case(99, L=2, H=2, g=2, d=128, T=T, Tq=76, dtype=torch.bfloat16, q_pos=q_pos)
+    ramp = torch.linspace(0.2, 24.0, T, device="cuda").to(torch.bfloat16)[None, None, :, None]
+    c.ka = (c.ka * ramp).contiguous()  # later keys score higher: the reference maximum rises
+    c.kb = (c.kb * ramp).contiguous()
+    c.h[1], c.h[3] = to_host64(c.ka), to_host64(c.kb)
+    got = c.gpu(kvb, _ctx(kvb, 2, 2, 128))
+    assert np.abs(got - c.oracle()).max() <= TOL_COS
+
+
 def test_identical_caches_give_one(kvb):
     c = Case(92, L=1, H=2, g=2, d=128, T=130, Tq=130, dtype=torch.bfloat16, noise=0.0)
     got = c.gpu(kvb, _ctx(kvb, 1, 2, 128))

@@ -563,7 +563,8 @@ def run_gpu(args, rank, world, local_rank):
     # Every step copies its source cache and positions host -> device, maps, and copies the
     # mapped cache device -> host.  Steps are pipelined over args.e2e_buffers device buffer
     # sets: the copy-in of later steps and the copy-out of earlier ones run on their own
-    # streams while step i maps.
+    # streams while step i maps.  Each copy is split by layers over args.e2e_streams
+    # streams per direction, so that several copy engines share the host link.
     h_src_k = torch.empty(src_k.shape, dtype=src_k.dtype, pin_memory=True)
     h_src_v = torch.empty(src_v.shape, dtype=src_v.dtype, pin_memory=True)
     h_pos = torch.empty(pos.shape, dtype=pos.dtype, pin_memory=True)
@@ -578,37 +579,55 @@ def run_gpu(args, rank, world, local_rank):
     bufs = [(src_k, src_v, pos, out_k, out_v)] + [
         (torch.empty_like(src_k), torch.empty_like(src_v), torch.empty_like(pos), torch.empty_like(out_k),
          torch.empty_like(out_v)) for _ in range(nbuf - 1)]
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n_str = max(1, args.e2e_streams)
+    s_in = [torch.cuda.Stream(dev) for _ in range(n_str)]
+    s_out = [torch.cuda.Stream(dev) for _ in range(n_str)]
+
+    def parts(n_layers):  # layer ranges of the n_str copies of one tensor
+        cut = [round(j * n_layers / n_str) for j in range(n_str + 1)]
+        return [(cut[j], cut[j + 1]) for j in range(n_str)]
+
+    in_parts, out_parts = parts(h_src_k.shape[0]), parts(h_out_k.shape[0])
 
     def run_e2e(n_steps, start_event):
-        s_in.wait_event(start_event)
-        s_out.wait_event(start_event)
-        ev_comp, ev_out = [None] * nbuf, [None] * nbuf
+        for st in s_in + s_out:
+            st.wait_event(start_event)
+        ev_comp, ev_out = [None] * nbuf, [[] for _ in range(nbuf)]
         for i in range(n_steps):
             b = i % nbuf
             sk, sv, ps, ok, ov = bufs[b]
-            with torch.cuda.stream(s_in):
-                if ev_comp[b] is not None:  # the map that last read this buffer is done
-                    s_in.wait_event(ev_comp[b])
-                sk.copy_(h_src_k, non_blocking=True)
-                sv.copy_(h_src_v, non_blocking=True)
-                ps.copy_(h_pos, non_blocking=True)
-                ev_in = torch.cuda.Event()
-                ev_in.record(s_in)
-            stream.wait_event(ev_in)
-            if ev_out[b] is not None:  # this output buffer has been copied out
-                stream.wait_event(ev_out[b])
+            ev_in = []
+            for j, st in enumerate(s_in):
+                with torch.cuda.stream(st):
+                    if ev_comp[b] is not None:  # the map that last read this buffer is done
+                        st.wait_event(ev_comp[b])
+                    a, e = in_parts[j]
+                    sk[a:e].copy_(h_src_k[a:e], non_blocking=True)
+                    sv[a:e].copy_(h_src_v[a:e], non_blocking=True)
+                    if j == 0:
+                        ps.copy_(h_pos, non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(st)
+                    ev_in.append(ev)
+            for ev in ev_in:
+                stream.wait_event(ev)
+            for ev in ev_out[b]:  # this output buffer has been copied out
+                stream.wait_event(ev)
             kvb.kvb_map_apply(ctx, sk, sv, ps, sel_k, sel_v, W_k, W_v, b_k, b_v, ok, ov, stream)
             ev_comp[b] = torch.cuda.Event()
             ev_comp[b].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_comp[b])
-                h_out_k.copy_(ok, non_blocking=True)
-                h_out_v.copy_(ov, non_blocking=True)
-                ev_out[b] = torch.cuda.Event()
-                ev_out[b].record(s_out)
-        stream.wait_stream(s_in)
-        stream.wait_stream(s_out)
+            ev_out[b] = []
+            for j, st in enumerate(s_out):
+                with torch.cuda.stream(st):
+                    st.wait_event(ev_comp[b])
+                    a, e = out_parts[j]
+                    h_out_k[a:e].copy_(ok[a:e], non_blocking=True)
+                    h_out_v[a:e].copy_(ov[a:e], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(st)
+                    ev_out[b].append(ev)
+        for st in s_in + s_out:
+            stream.wait_stream(st)
 
     e2e_steps = max(2, args.steps)
     warm = torch.cuda.Event()
@@ -701,7 +720,7 @@ def run_gpu(args, rank, world, local_rank):
                 "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
                 "how": "kvb_map_apply on device copies of pinned host caches; per step H2D of source K/V + "
                        "positions and D2H of target K/V; steps pipelined on copy/compute streams over "
-                       f"{nbuf} device buffer sets"},
+                       f"{nbuf} device buffer sets, each copy split by layers over {n_str} stream(s) per direction"},
         "fit": fit,
         "attention_cosine": attn_roofline(attn, clk),
         "fp32_map": fp32_map,
@@ -730,6 +749,8 @@ def main():
     ap.add_argument("--fit-f32", action="store_true", help="fit leg with fp32 caches (with --fit-only)")
     ap.add_argument("--e2e-buffers", type=int, default=2,
                     help="device buffer sets the end-to-end leg pipelines its steps over")
+    ap.add_argument("--e2e-streams", type=int, default=1,
+                    help="streams per copy direction in the end-to-end leg (each copy split by layers)")
     ap.add_argument("--fit-block", type=int, default=0,
                     help="fit leg with statistics of this many target layers at a time (one pass per block)")
     args = ap.parse_args()

@@ -83,18 +83,18 @@ struct Params {
 };
 
 struct Maps {
-    CUtensorMap a_hi[4], a_lo[4], a_3[4], b_hi[4], b_lo[4], b_3[4];
+    CUtensorMap a[3][4], b[3][4];  // [part: hi, lo, third][job]
 };
 
 // Operand parts of product `seg`, largest first: two-part operands take
 // hi.hi, hi.lo, lo.hi; three-part operands add hi.3, lo.lo, 3.hi (every product
-// down to 2^-16 of the leading one).
+// down to 2^-16 of the leading one).  The part indices are packed four bits per
+// product so that the single producer thread computes them in registers.
 __device__ __forceinline__ void product_maps(const Maps& M, int job, int seg, const CUtensorMap*& ma,
                                              const CUtensorMap*& mb) {
-    constexpr int pa[6] = {0, 0, 1, 0, 1, 2}, pb[6] = {0, 1, 0, 2, 1, 0};
-    const int a = pa[seg], b = pb[seg];
-    ma = a == 0 ? &M.a_hi[job] : a == 1 ? &M.a_lo[job] : &M.a_3[job];
-    mb = b == 0 ? &M.b_hi[job] : b == 1 ? &M.b_lo[job] : &M.b_3[job];
+    constexpr uint32_t PA = 0x210100u, PB = 0x012010u;  // parts of A and B for products 0..5
+    ma = &M.a[(PA >> (4 * seg)) & 3u][job];
+    mb = &M.b[(PB >> (4 * seg)) & 3u][job];
 }
 
 __device__ __forceinline__ void decode(uint32_t e, int& job, int& bi, int& bj) {
@@ -612,12 +612,12 @@ cudaError_t launch_stats_gemm_tc(StatsGemmPlan* plan, const StatsJob* jobs, int 
     P.nprod = jobs[0].A_3 ? 6 : 3;
     for (int j = 0; j < n_jobs; ++j) {
         const StatsJob& J = jobs[j];
-        if (J.A_3 && (!encode_2d(&M.a_3[j], J.A_3, ld, J.Ma, BM, why) ||
-                      !encode_2d(&M.b_3[j], J.B_3, ld, J.Nb, pair ? 128 : BN, why)))
+        if (J.A_3 && (!encode_2d(&M.a[2][j], J.A_3, ld, J.Ma, BM, why) ||
+                      !encode_2d(&M.b[2][j], J.B_3, ld, J.Nb, pair ? 128 : BN, why)))
             return cudaErrorInvalidValue;
-        if (!encode_2d(&M.a_hi[j], J.A, ld, J.Ma, BM, why) || !encode_2d(&M.a_lo[j], J.A_lo, ld, J.Ma, BM, why) ||
-            !encode_2d(&M.b_hi[j], J.B, ld, J.Nb, pair ? 128 : BN, why) ||
-            !encode_2d(&M.b_lo[j], J.B_lo, ld, J.Nb, pair ? 128 : BN, why))
+        if (!encode_2d(&M.a[0][j], J.A, ld, J.Ma, BM, why) || !encode_2d(&M.a[1][j], J.A_lo, ld, J.Ma, BM, why) ||
+            !encode_2d(&M.b[0][j], J.B, ld, J.Nb, pair ? 128 : BN, why) ||
+            !encode_2d(&M.b[1][j], J.B_lo, ld, J.Nb, pair ? 128 : BN, why))
             return cudaErrorInvalidValue;
         P.job[j] = JobP{J.out, J.da, J.db, J.za, J.zb, J.ldo};
     }

@@ -183,15 +183,27 @@ __device__ __forceinline__ bool strip_while_waiting(const Params& P, uint64_t* t
 }
 
 // K-block kb of target layer t: (source layer, head, first dim) of its box.
-__device__ __forceinline__ void kblock_source(const Params& P, int kv, int t, int kb, int q, int& layer, int& h,
-                                              int& e0) {
-    const int f0 = kb * BK;
-    const int j = f0 / q;
-    const int rem = f0 - j * q;
-    h = rem / P.d;
-    e0 = rem - h * P.d;
-    layer = P.sel.s[kv][t][j];
-}
+// Source of consecutive K blocks of one (kv, target layer) problem: feature
+// (j * H + h) * d + e is dim e of head h of the j-th selected source layer.  The
+// producer steps it BK features at a time (BK divides d), without divisions.
+struct KSrc {
+    int j, h, e0, slab;  // slab: the source layer's first (layer, head) slab
+    __device__ __forceinline__ void start(const Params& P, int kv, int t) {
+        j = h = e0 = 0;
+        slab = P.sel.s[kv][t][0] * P.H;
+    }
+    __device__ __forceinline__ void next(const Params& P, int kv, int t) {
+        e0 += BK;
+        if (e0 == P.d) {
+            e0 = 0;
+            if (++h == P.H) {
+                h = 0;
+                ++j;
+                slab = P.sel.s[kv][t][j < MAX_K ? j : MAX_K - 1] * P.H;  // past the last: never used
+            }
+        }
+    }
+};
 
 // One thread's row of one accumulator tile (256 columns = two heads): bias,
 // target RoPE for keys, bf16 rounding (or fp32 as is), store into [t][h][tok][e].
@@ -361,9 +373,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!wait_strip_done(P, abort_flag)) break;
                     stripped = true;
                 }
+                KSrc src;
+                src.start(P, c.kv, c.t);
+                int kb = 0, seg = 0;  // seg 0: hi x hi, 1: hi x lo, 2: lo x hi
                 for (int ki = 0; ki < nk_issue; ++ki) {
-                    const int kb = SPLIT ? ki / 3 : ki;
-                    const int seg = SPLIT ? ki - 3 * kb : 0;  // 0: hi x hi, 1: hi x lo, 2: lo x hi
                     const CUtensorMap* ta = seg == 2 ? (c.kv ? &tm_a1l : &tm_a0l) : (c.kv ? &tm_a1 : &tm_a0);
                     const CUtensorMap* tw = seg == 1 ? (c.kv ? &tm_w1l : &tm_w0l) : (c.kv ? &tm_w1 : &tm_w0);
                     if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) {
@@ -371,10 +384,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                    int layer, h, e0;
-                    kblock_source(P, c.kv, c.t, kb, q, layer, h, e0);
-                    tma_load_3d(sA + stage * A_BYTES, ta, &full[stage], e0, c.m * BM, layer * P.H + h);
+                    tma_load_3d(sA + stage * A_BYTES, ta, &full[stage], src.e0, c.m * BM, src.slab + src.h);
                     tma_load_3d(sB + stage * B_BYTES, tw, &full[stage], kb * BK, c.n * BN, c.t);
+                    if (!SPLIT || seg == 2) {
+                        src.next(P, c.kv, c.t);
+                        ++kb;
+                        seg = 0;
+                    } else {
+                        ++seg;
+                    }
                     issued_phase[stage] = static_cast<int>(phase);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -590,9 +608,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!wait_strip_done(P, abort_flag)) break;
                     stripped = true;
                 }
+                KSrc src;
+                src.start(P, c.kv, c.t);
+                int kb = 0, seg = 0;  // seg 0: hi x hi, 1: hi x lo, 2: lo x hi
                 for (int ki = 0; ki < P.nk * NSEG; ++ki) {
-                    const int kb = SPLIT ? ki / 3 : ki;
-                    const int seg = SPLIT ? ki - 3 * kb : 0;  // 0: hi x hi, 1: hi x lo, 2: lo x hi
                     const CUtensorMap* ta = seg == 2 ? (c.kv ? &tm_a1l : &tm_a0l) : (c.kv ? &tm_a1 : &tm_a0);
                     const CUtensorMap* tw = seg == 1 ? (c.kv ? &tm_w1l : &tm_w0l) : (c.kv ? &tm_w1 : &tm_w0);
                     if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) {
@@ -601,11 +620,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * PSTAGE_BYTES);
-                    int layer, h, e0;
-                    kblock_source(P, c.kv, c.t, kb, q, layer, h, e0);
-                    tma_load_3d_pair(sA + stage * PA_BYTES, ta, full_leader, e0, c.m * PM + 128 * rank,
-                                     layer * P.H + h);
+                    tma_load_3d_pair(sA + stage * PA_BYTES, ta, full_leader, src.e0, c.m * PM + 128 * rank,
+                                     src.slab + src.h);
                     tma_load_3d_pair(sB + stage * PB_BYTES, tw, full_leader, kb * BK, c.n * BN + 128 * rank, c.t);
+                    if (!SPLIT || seg == 2) {
+                        src.next(P, c.kv, c.t);
+                        ++kb;
+                        seg = 0;
+                    } else {
+                        ++seg;
+                    }
                     issued_phase[stage] = static_cast<int>(phase);
                     if (++stage == PSTAGES) {
                         stage = 0;

@@ -209,18 +209,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int t = blockIdx.x; ok && t < P.n_tiles; t += gridDim.x) {
                 int job, bi, bj;
                 decode(P.tiles[t], job, bi, bj);
-                for (int it = 0; it < iters; ++it) {
+                const CUtensorMap *ma, *mb;
+                product_maps(M, job, 0, ma, mb);
+                for (int it = 0, seg = 0, kb = 0; it < iters; ++it) {  // it = seg * nk + kb
                     if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const int seg = it / nk;
-                    const int kb = it - seg * nk;
-                    const CUtensorMap *ma, *mb;
-                    product_maps(M, job, seg, ma, mb);
                     mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
                     tma_load_2d(sA + stage * A_BYTES, ma, &full[stage], kb * BK, bi * BM);
                     tma_load_2d(sB + stage * B_BYTES, mb, &full[stage], kb * BK, bj * BN);
+                    if (++kb == nk && ++seg < P.nprod) {
+                        kb = 0;
+                        product_maps(M, job, seg, ma, mb);
+                    }
                     issued_phase[stage] = static_cast<int>(phase);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -416,19 +418,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (t >= P.n_tiles) break;
                 int job, bi, bj;
                 decode(P.tiles[t], job, bi, bj);
-                for (int it = 0; it < iters; ++it) {
+                const CUtensorMap *ma, *mb;
+                product_maps(M, job, 0, ma, mb);
+                for (int it = 0, seg = 0, kb = 0; it < iters; ++it) {  // it = seg * nk + kb
                     if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const int seg = it / nk;
-                    const int kb = it - seg * nk;
-                    const CUtensorMap *ma, *mb;
-                    product_maps(M, job, seg, ma, mb);
                     const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * PSTAGE_BYTES);
                     tma_load_2d_pair(sA + stage * PA_BYTES, ma, full_leader, kb * BK, bi * PM + 128 * rank);
                     tma_load_2d_pair(sB + stage * PA_BYTES, mb, full_leader, kb * BK, bj * PM + 128 * rank);
+                    if (++kb == nk && ++seg < P.nprod) {
+                        kb = 0;
+                        product_maps(M, job, seg, ma, mb);
+                    }
                     issued_phase[stage] = static_cast<int>(phase);
                     if (++stage == PSTAGES) {
                         stage = 0;

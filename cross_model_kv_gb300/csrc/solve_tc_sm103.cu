@@ -46,9 +46,11 @@ constexpr int TMEM_COLS = 256;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr uint64_t DRAIN_NS = 200ull * 1000 * 1000;
 constexpr int NPROD = 6;
-// part of A and of B in each of the six products, largest first
-__constant__ int kPartA[NPROD] = {0, 0, 1, 0, 1, 2};
-__constant__ int kPartB[NPROD] = {0, 1, 0, 2, 1, 0};
+// part of A and of B in each of the six products, largest first, four bits per
+// product (A 0,0,1,0,1,2 and B 0,1,0,2,1,0), so that the producer needs no table
+constexpr uint32_t kPartsA = 0x210100u, kPartsB = 0x012010u;
+__device__ __forceinline__ int part_a(int pr) { return static_cast<int>((kPartsA >> (4 * pr)) & 3u); }
+__device__ __forceinline__ int part_b(int pr) { return static_cast<int>((kPartsB >> (4 * pr)) & 3u); }
 
 struct Params {
     float* C;
@@ -115,8 +117,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 2) solve_gemm_kernel(const __grid
                 const int kb = it / NPROD, pr = it - kb * NPROD;
                 if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) break;
                 mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                tma_load_3d(sA + stage * A_BYTES, &Mp.a[kPartA[pr]], &full[stage], kb * BK, m0, bz);
-                tma_load_3d(sB + stage * B_BYTES, &Mp.b[kPartB[pr]], &full[stage], kb * BK, n0, bz);
+                tma_load_3d(sA + stage * A_BYTES, &Mp.a[part_a(pr)], &full[stage], kb * BK, m0, bz);
+                tma_load_3d(sB + stage * B_BYTES, &Mp.b[part_b(pr)], &full[stage], kb * BK, n0, bz);
                 issued_phase[stage] = static_cast<int>(phase);
                 if (++stage == STAGES) {
                     stage = 0;
@@ -306,8 +308,8 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1) solve_gemm_persistent_kernel(
                         break;
                     }
                     mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                    tma_load_3d(sA + stage * A_BYTES, &Mp.a[kPartA[pr]], &full[stage], kb * BK, mi * BM, bz);
-                    tma_load_3d(sB + stage * B_BYTES, &Mp.b[kPartB[pr]], &full[stage], kb * BK, nj * BN, bz);
+                    tma_load_3d(sA + stage * A_BYTES, &Mp.a[part_a(pr)], &full[stage], kb * BK, mi * BM, bz);
+                    tma_load_3d(sB + stage * B_BYTES, &Mp.b[part_b(pr)], &full[stage], kb * BK, nj * BN, bz);
                     issued_phase[stage] = static_cast<int>(phase);
                     if (++stage == PSTAGES) {
                         stage = 0;

@@ -75,6 +75,18 @@ def test_bf16_tensor_core_single_token(kvb):
     _check_all(kvb, c, 8, TOL_BF16)
 
 
+@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_tensor_core_largest_top_k(kvb, monkeypatch, pair, dtype):
+    # top_k = 16, the most a context takes: the producer steps through 16 selected
+    # source layers x 2 heads x 2 K blocks per head (and past the last selection
+    # entry after the final block), on the CTA-pair and the single-CTA kernels
+    monkeypatch.setenv("KVB_MAP_PAIR", pair)
+    dt, tol = (torch.bfloat16, TOL_BF16) if dtype == "bf16" else (torch.float32, TOL_F32)
+    c = ApplyCase(17, 3, 2, 128, 16, 300, 1e4, 1e6, dt, seed=26)
+    _check_all(kvb, c, 512, tol)
+
+
 def test_bf16_cuda_core_path_head_dim_64(kvb):
     c = ApplyCase(3, 2, 4, 64, 2, 200, 1e4, 1e6, torch.bfloat16, seed=24)
     _check_all(kvb, c, 256, TOL_BF16)

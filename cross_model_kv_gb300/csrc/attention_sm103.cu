@@ -11,7 +11,8 @@
 // One CTA per (layer, KV head, 128 query rows of the head's query group), one
 // CTA per SM (all 512 TMEM columns).  The two caches run side by side, each
 // with its own producer, MMA issuer and softmax warpgroup; for every 128-key
-// tile that some row of the CTA may see:
+// tile that some row of the CTA may see (and always the first, whose copies
+// start at entry):
 //   warps 0, 1   TMA (cache a, b): the key tile and the value tile, each as two
 //                64-wide 128-byte-swizzled boxes;
 //   warps 2, 3   tcgen05.mma (cache a, b): S = Q K^T into TMEM (M 128, N 128,
@@ -157,6 +158,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive_expect_tx(q_full, TILE);
         tma_load_2d(sQ, &Mp.q, q_full, 0, qrow0);
         tma_load_2d(sQ + ATOM, &Mp.q, q_full, 64, qrow0);
+        // key tile 0 counts as live for every row block (a tile that no row sees only
+        // adds zero probabilities), so both caches' first key and value tiles are copied
+        // now, while TMEM is allocated and the other tiles are flagged
+        for (int x = 0; x < 2; ++x) {
+            mbar_arrive_expect_tx(&kv_full[x], 2 * TILE);
+            tma_load_3d(sK(x), &Mp.k[x], &kv_full[x], 0, 0, slab);
+            tma_load_3d(sK(x) + ATOM, &Mp.k[x], &kv_full[x], 64, 0, slab);
+            tma_load_3d(sV(x), &Mp.v[x], &kv_full[x], 0, 0, slab);
+            tma_load_3d(sV(x) + ATOM, &Mp.v[x], &kv_full[x], 64, 0, slab);
+        }
     }
     if (warp == 2) {
         tmem_alloc(tmem_slot, 512);
@@ -192,7 +203,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    auto live = [&](int t) { return !use_flags || flags[t] != 0; };
+    auto live = [&](int t) { return t == 0 || !use_flags || flags[t] != 0; };
 
     if (warp < 2) {
         if (lane == 0) {
@@ -201,6 +212,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int it = 0, last = -1;
             for (int t = 0; t < ntiles; ++t) {
                 if (!live(t)) continue;
+                if (t == 0) {  // copied at entry
+                    last = it++;
+                    continue;
+                }
                 if (!mbar_wait(&kv_empty[x], (it & 1) ^ 1u, P.err, abort_flag)) break;
                 mbar_arrive_expect_tx(&kv_full[x], 2 * TILE);
                 tma_load_3d(sK(x), &Mp.k[x], &kv_full[x], 0, t * TK, slab);

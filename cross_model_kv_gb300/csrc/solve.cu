@@ -265,6 +265,73 @@ __global__ void __launch_bounds__(256) potrf_diag_kernel(float* G, int64_t ldg, 
     }
 }
 
+// In place, X <- A X for one block of nb <= 64 right-hand-side rows (row stride
+// ldc) and the inverse of its diagonal block, A(i, k) = Lb[i * NB + k], or that
+// inverse transposed, A(i, k) = Lb[k * NB + i]: the triangular solves' diagonal
+// steps.  One CTA per 256 columns of one system holds the 64 x 64 block and its
+// 64 x 256 slab of X in shared memory (the slab is read whole before any of it is
+// written back); each thread owns 8 rows x 8 columns (columns 4c..4c+3 and
+// 128+4c..128+4c+3, so that a quarter warp's 16-byte reads cover all banks).
+constexpr int DA_COLS = 256;
+constexpr int DA_LDA = NB + 4;  // padded row of the block in shared memory (16-byte aligned)
+constexpr int DA_SMEM = (NB * DA_LDA + NB * DA_COLS) * 4;
+
+__global__ void __launch_bounds__(256, 2) diag_apply_kernel(const float* __restrict__ Linv, int64_t strideL,
+                                                           float* __restrict__ C, int64_t ldc, int64_t strideC,
+                                                           int nb, int64_t m, int transpose) {
+    extern __shared__ __align__(16) float dsm[];
+    float* sa = dsm;              // sa[k * DA_LDA + i] = A(i, k)
+    float* sx = dsm + NB * DA_LDA;  // sx[k * DA_COLS + c] = X(k, c0 + c)
+    const int b = blockIdx.y;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * DA_COLS;
+    const float* Lb = Linv + b * strideL;
+    float* X = C + b * strideC;
+    for (int e = threadIdx.x; e < NB * NB; e += blockDim.x) {
+        const int r = e / NB, q = e - r * NB;  // Lb element (r, q), read in order
+        const float v = (r < nb && q < nb) ? Lb[r * NB + q] : 0.f;
+        if (transpose)
+            sa[r * DA_LDA + q] = v;  // A(q, r) = Lb[r * NB + q]
+        else
+            sa[q * DA_LDA + r] = v;  // A(r, q) = Lb[r * NB + q]
+    }
+    for (int e = threadIdx.x; e < NB * (DA_COLS / 4); e += blockDim.x) {
+        const int k = e / (DA_COLS / 4), c = 4 * (e - k * (DA_COLS / 4));
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < nb && c0 + c < m) v = *reinterpret_cast<const float4*>(X + k * ldc + c0 + c);
+        *reinterpret_cast<float4*>(sx + k * DA_COLS + c) = v;
+    }
+    __syncthreads();
+    const int r0 = 8 * (threadIdx.x >> 5);
+    const int cx = 4 * (threadIdx.x & 31);
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < nb; ++k) {
+        const float4 a0 = *reinterpret_cast<const float4*>(sa + k * DA_LDA + r0);
+        const float4 a1 = *reinterpret_cast<const float4*>(sa + k * DA_LDA + r0 + 4);
+        const float4 x0 = *reinterpret_cast<const float4*>(sx + k * DA_COLS + cx);
+        const float4 x1 = *reinterpret_cast<const float4*>(sx + k * DA_COLS + 128 + cx);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], xv[j], acc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = r0 + i;
+        if (r >= nb) break;
+        float* row = X + r * ldc + c0;
+        if (c0 + cx < m) *reinterpret_cast<float4*>(row + cx) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        if (c0 + 128 + cx < m)
+            *reinterpret_cast<float4*>(row + 128 + cx) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_f32(const GemmArgs& g, cudaStream_t s) {
@@ -377,6 +444,17 @@ cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int
     // Block row j of C times the inverse diagonal block (or its transpose), in place:
     // every output column depends only on the same column of the block row.
     auto diag = [&](int64_t j0, int nb, bool transpose) {
+        const bool vec = m % 4 == 0 && ldc % 4 == 0 && strideC % 4 == 0 && strideL % 4 == 0 &&
+                         (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (reinterpret_cast<uintptr_t>(Linv) & 15u) == 0;
+        if (vec) {
+            const cudaError_t ea =
+                cudaFuncSetAttribute(diag_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DA_SMEM);
+            if (ea != cudaSuccess) return ea;
+            dim3 grid(static_cast<unsigned>((m + DA_COLS - 1) / DA_COLS), static_cast<unsigned>(batch));
+            diag_apply_kernel<<<grid, 256, DA_SMEM, s>>>(Linv + j0 * NB, strideL, C + j0 * ldc, ldc, strideC, nb, m,
+                                                         transpose ? 1 : 0);
+            return cudaGetLastError();
+        }
         GemmArgs t{};
         t.A = Linv + j0 * NB;
         t.B = C + j0 * ldc;

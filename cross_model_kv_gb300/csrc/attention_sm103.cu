@@ -261,7 +261,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Two threads per row (warps w and w + 4 share a TMEM lane quarter): this one
         // takes keys kh0 .. kh0+63 of every tile and output dims kh0 .. kh0+63.  The two
         // halves exchange tile maxima (and, at the end, the cosine's sums) through the
-        // cache's P-lo tile, which no MMA reads at those points.  The eight warps of a
+        // cache's P-lo tile, which no MMA reads at those points.  A thread's maximum goes
+        // into the first 16 bytes of its partner's own P-lo chunks of the row: the partner
+        // reads it before its pass 2 overwrites them, and the next maximum is written
+        // only once the next S is ready, after O += P V has read P lo.  The eight warps of a
         // cache meet at named barrier 1 + x; whether to go on is agreed there first
         // (every wait before it is bounded), so no warp leaves while others wait.
         const int x = gx;
@@ -269,7 +272,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int bar_id = 1 + x;
         const uint32_t tl = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         const uint32_t cS = 128u * x + kh0, cO = 256u + 128u * x + kh0;
-        float* xch = reinterpret_cast<float*>(sPl(x));  // [2][128] exchange slots
+        float* xch = reinterpret_cast<float*>(sPl(x));  // [3][128] cosine-sum slots (at the end)
+        float* slot_in = reinterpret_cast<float*>(sPl(x) + sw_off(row, 8 * hf));         // the partner's maximum
+        float* slot_out = reinterpret_cast<float*>(sPl(x) + sw_off(row, 8 * (1 - hf)));  // this thread's
         auto wait_all = [&](uint64_t* b, uint32_t parity) {  // warp-uniform outcome
             const bool got = mbar_wait(b, parity, P.err, abort_flag);
             return __all_sync(0xffffffffu, got);
@@ -316,10 +321,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if ((vis[kk >> 5] >> (kk & 31)) & 1u) mt = fmaxf(mt, __uint_as_float(sv[c][u]));
                     }
             }
-            xch[hf * 128 + row] = mt;
+            *slot_out = mt;
             named_bar_sync(bar_id, 256);
-            mt = fmaxf(mt, xch[(1 - hf) * 128 + row]) * P.scale_log2;  // scale > 0: commutes with the maximum
-            named_bar_sync(bar_id, 256);  // both halves read before P lo overwrites the slots
+            mt = fmaxf(mt, *slot_in) * P.scale_log2;  // scale > 0: commutes with the maximum
             const bool raise = mt > m_ref + RESCALE_LOG2;  // also the first visible tile of the row
             if (__any_sync(0xffffffffu, raise && it > 0 && m_ref > -INFINITY)) {
                 // O was accumulated against the old reference: rescale this half in TMEM

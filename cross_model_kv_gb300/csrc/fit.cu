@@ -38,51 +38,68 @@ __global__ void gather_system_kernel(const float* __restrict__ M, int64_t ldm, S
     if (j == 0) D[b * n + i] = di;
 }
 
-// Same values as gather_system_kernel, 32 x 32 tiles of G per block (q a
-// multiple of 32, so a tile's rows, and its columns, are 32 consecutive
-// features of one layer).  A tile whose row and column features do not overlap
-// lies wholly in the stored lower triangle or wholly above it: it is read as
-// 32 coalesced rows of M, either directly or transposed through shared memory.
-// Tiles whose feature ranges overlap take the element-wise path.
+// D[b][i] = 1 / sqrt(M_ii + lambda), once per system, for the tiled gather below.
+__global__ void jacobi_scale_kernel(const float* __restrict__ M, int64_t ldm, SysLayers L, int q, int64_t n,
+                                    float lambda, float* __restrict__ D) {
+    const int b = blockIdx.y;
+    const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (i >= n) return;
+    const int64_t fi = feat_index(L, b, i, q);
+    D[b * n + i] = rsqrtf(M[fi * (ldm + 1)] + lambda);
+}
+
+// Same values as gather_system_kernel from 32 x 32 tiles of G (q a multiple of
+// 32, so a tile's rows, and its columns, are 32 consecutive features of one
+// layer), GS_TILES tiles of one tile row per block, with the scales D computed
+// beforehand.  A tile whose row and column features do not overlap lies wholly
+// in the stored lower triangle or wholly above it: it is read as 32 coalesced
+// rows of M, either directly or transposed through shared memory.  Tiles whose
+// feature ranges overlap take the element-wise path.
+constexpr int GS_TILES = 8;
+
 __global__ void __launch_bounds__(256) gather_system_tiled_kernel(const float* __restrict__ M, int64_t ldm,
                                                                   SysLayers L, int q, int64_t n, float lambda,
                                                                   float* __restrict__ G, int64_t strideG,
-                                                                  float* __restrict__ D) {
+                                                                  const float* __restrict__ D) {
     __shared__ float tile[32][33];
     __shared__ float di_s[32], dj_s[32];
     const int b = blockIdx.z;
-    const int64_t i0 = static_cast<int64_t>(blockIdx.y) * 32, j0 = static_cast<int64_t>(blockIdx.x) * 32;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.y) * 32;
     const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-    const int64_t fi0 = feat_index(L, b, i0, q), fj0 = feat_index(L, b, j0, q);
-    if (ty == 0) {
-        di_s[tx] = i0 + tx < n ? rsqrtf(M[(fi0 + tx) * (ldm + 1)] + lambda) : 0.f;
-        dj_s[tx] = j0 + tx < n ? rsqrtf(M[(fj0 + tx) * (ldm + 1)] + lambda) : 0.f;
-    }
-    const bool lower = fi0 >= fj0 + 32, upper = fj0 >= fi0 + 32;
-    if (lower || upper) {
+    const int64_t fi0 = feat_index(L, b, i0, q);
+    if (ty == 0) di_s[tx] = i0 + tx < n ? D[b * n + i0 + tx] : 0.f;
+#pragma unroll 1
+    for (int t = 0; t < GS_TILES; ++t) {
+        const int64_t j0 = (static_cast<int64_t>(blockIdx.x) * GS_TILES + t) * 32;
+        if (j0 >= n) break;  // uniform over the block
+        const int64_t fj0 = feat_index(L, b, j0, q);
+        __syncthreads();  // the previous tile is stored (and di_s is visible)
+        if (ty == 1) dj_s[tx] = j0 + tx < n ? D[b * n + j0 + tx] : 0.f;
+        const bool lower = fi0 >= fj0 + 32, upper = fj0 >= fi0 + 32;
+        if (lower || upper) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int r = ty + 8 * k;
+                // lower: row fi0 + r of M, columns fj0 ..; upper: row fj0 + r, columns fi0 ..
+                const bool in = lower ? (i0 + r < n && j0 + tx < n) : (j0 + r < n && i0 + tx < n);
+                tile[r][tx] = in ? (lower ? M[(fi0 + r) * ldm + fj0 + tx] : M[(fj0 + r) * ldm + fi0 + tx]) : 0.f;
+            }
+        }
+        __syncthreads();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int r = ty + 8 * k;
-            // lower: row fi0 + r of M, columns fj0 ..; upper: row fj0 + r, columns fi0 ..
-            const bool in = lower ? (i0 + r < n && j0 + tx < n) : (j0 + r < n && i0 + tx < n);
-            tile[r][tx] = in ? (lower ? M[(fi0 + r) * ldm + fj0 + tx] : M[(fj0 + r) * ldm + fi0 + tx]) : 0.f;
+            const int64_t i = i0 + r, j = j0 + tx;
+            if (i >= n || j >= n) continue;
+            float v;
+            if (lower)
+                v = tile[r][tx];
+            else if (upper)
+                v = tile[tx][r];
+            else
+                v = gram_at(M, ldm, fi0 + r, fj0 + tx) + (i == j ? lambda : 0.f);
+            G[b * strideG + i * n + j] = di_s[r] * v * dj_s[tx];
         }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int r = ty + 8 * k;
-        const int64_t i = i0 + r, j = j0 + tx;
-        if (i >= n || j >= n) continue;
-        float v;
-        if (lower)
-            v = tile[r][tx];
-        else if (upper)
-            v = tile[tx][r];
-        else
-            v = gram_at(M, ldm, fi0 + r, fj0 + tx) + (i == j ? lambda : 0.f);
-        G[b * strideG + i * n + j] = di_s[r] * v * dj_s[tx];
-        if (j == 0) D[b * n + i] = di_s[r];
     }
 }
 
@@ -207,7 +224,10 @@ cudaError_t launch_gather_system(const float* M, int64_t ldm, const SysLayers& L
                                  float* G, int64_t strideG, float* D, int batch, cudaStream_t s) {
     dim3 blk(32, 8);
     if (q % 32 == 0) {
-        dim3 grid(static_cast<unsigned>((n + 31) / 32), static_cast<unsigned>((n + 31) / 32), batch);
+        jacobi_scale_kernel<<<dim3(static_cast<unsigned>((n + 255) / 256), batch), 256, 0, s>>>(M, ldm, L, q, n,
+                                                                                                 lambda, D);
+        const int64_t tiles = (n + 31) / 32;
+        dim3 grid(static_cast<unsigned>((tiles + GS_TILES - 1) / GS_TILES), static_cast<unsigned>(tiles), batch);
         gather_system_tiled_kernel<<<grid, blk, 0, s>>>(M, ldm, L, q, n, lambda, G, strideG, D);
         return cudaGetLastError();
     }

@@ -475,6 +475,37 @@ cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int
         return launch_gemm_f32(t, s);
     };
     cudaError_t e;
+    // With many right-hand sides the updates read the super-block's rows of C as
+    // their B operand on the tensor cores; each 64-row block is then split into
+    // its bf16 parts once, right after its diagonal step (the rows are final for
+    // the rest of the pass), into a cache after the A operand's part of the update
+    // workspace, and every update reads the cache from the block's column on.
+    const bool cached = tc && tc->ws && tc_update_supported(tc, NB, m, SP, C, ldc) &&
+                        tc->ws_bytes >= tc_update_ws_bytes(n, m, batch);
+    TcPreSplit cache{};
+    if (cached) {
+        cache.ld = SP;
+        cache.part = static_cast<int64_t>(batch) * m * SP;
+        cache.base = tc->ws + 3 * static_cast<int64_t>(batch) * n * SP;  // past the A parts (rows <= n, K <= SP)
+    }
+    auto split_rows = [&](int64_t k0, int64_t j0, int nb) {  // rows j0 .. j0+nb of C into cache columns j0 - k0 ..
+        TcPreSplit d = cache;
+        d.base += j0 - k0;
+        return tc_split_into(TcOperand{C + j0 * ldc, m, 1, ldc, strideC}, nb, batch, d, s);
+    };
+    // C rows (Cd) -= A (M x K) times the K cached rows from cache column col0 on
+    auto update_rhs = [&](const float* A, int64_t a_row, int64_t a_k, int64_t M, int64_t col0, int64_t row0, int K,
+                          float* Cd) {
+        if (cached && tc_update_supported(tc, M, m, K, Cd, ldc)) {
+            TcPreSplit b = cache;
+            b.base += col0;
+            const TcOperand ao{A, M, a_row, a_k, strideG};
+            const TcOperand bo{C + row0 * ldc, m, 1, ldc, strideC};
+            return launch_tc_update(*tc, ao, &bo, K, Cd, ldc, strideC, -1.f, 1.f, false, batch, s, nullptr, &b);
+        }
+        return update(tc, A, a_row, a_k, strideG, M, C + row0 * ldc, 1, ldc, strideC, m, K, Cd, ldc, strideC, -1.f,
+                      1.f, false, batch, s);
+    };
     // forward, L Y = C, one super-block of rows at a time: each 64-row step takes
     // the earlier steps of its super-block, then its inverse diagonal block; then
     // one rank-(NSUB * 64) update of every row below.  B(k, n) = C[k][n]: row
@@ -484,15 +515,14 @@ cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int
         for (int64_t j0 = k0; j0 < kend; j0 += NB) {
             const int nb = static_cast<int>(kend - j0 < NB ? kend - j0 : NB);
             if (j0 > k0) {
-                e = update(tc, L + j0 * ldg + k0, ldg, 1, strideG, nb, C + k0 * ldc, 1, ldc, strideC, m,
-                           static_cast<int>(j0 - k0), C + j0 * ldc, ldc, strideC, -1.f, 1.f, false, batch, s);
+                e = update_rhs(L + j0 * ldg + k0, ldg, 1, nb, 0, k0, static_cast<int>(j0 - k0), C + j0 * ldc);
                 if (e != cudaSuccess) return e;
             }
             if ((e = diag(j0, nb, false)) != cudaSuccess) return e;
+            if (cached && (e = split_rows(k0, j0, nb)) != cudaSuccess) return e;
         }
         if (kend >= n) break;
-        e = update(tc, L + kend * ldg + k0, ldg, 1, strideG, n - kend, C + k0 * ldc, 1, ldc, strideC, m,
-                   static_cast<int>(kend - k0), C + kend * ldc, ldc, strideC, -1.f, 1.f, false, batch, s);
+        e = update_rhs(L + kend * ldg + k0, ldg, 1, n - kend, 0, k0, static_cast<int>(kend - k0), C + kend * ldc);
         if (e != cudaSuccess) return e;
     }
     // backward, L^T X = Y, last super-block first; inside it the last step first,
@@ -505,16 +535,15 @@ cudaError_t chol_solve_batched(const float* L, int64_t ldg, int64_t strideG, int
         for (int64_t j0 = k0 + ((kend - 1 - k0) / NB) * NB; j0 >= k0; j0 -= NB) {
             const int nb = static_cast<int>(kend - j0 < NB ? kend - j0 : NB);
             if (j0 + nb < kend) {
-                e = update(tc, L + (j0 + nb) * ldg + j0, 1, ldg, strideG, nb, C + (j0 + nb) * ldc, 1, ldc, strideC,
-                           m, static_cast<int>(kend - j0 - nb), C + j0 * ldc, ldc, strideC, -1.f, 1.f, false, batch,
-                           s);
+                e = update_rhs(L + (j0 + nb) * ldg + j0, 1, ldg, nb, j0 + nb - k0, j0 + nb,
+                               static_cast<int>(kend - j0 - nb), C + j0 * ldc);
                 if (e != cudaSuccess) return e;
             }
             if ((e = diag(j0, nb, true)) != cudaSuccess) return e;
+            if (cached && (e = split_rows(k0, j0, nb)) != cudaSuccess) return e;
         }
         if (k0 == 0) break;
-        e = update(tc, L + k0 * ldg, 1, ldg, strideG, k0, C + k0 * ldc, 1, ldc, strideC, m,
-                   static_cast<int>(kend - k0), C, ldc, strideC, -1.f, 1.f, false, batch, s);
+        e = update_rhs(L + k0 * ldg, 1, ldg, k0, 0, k0, static_cast<int>(kend - k0), C);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

@@ -438,10 +438,10 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1) solve_gemm_persistent_kernel(
 // [batch][rows][kp] with zeros beyond K.  Element (r, k) of batch item b is
 // src[b * s_batch + r * s_row + k * s_k]; 32 x 32 tiles through shared
 // memory so that both K-contiguous and row-contiguous sources read coalesced.
-__global__ void __launch_bounds__(256) split3_kernel(const float* __restrict__ src, int64_t rows, int K, int kp,
+__global__ void __launch_bounds__(256) split3_kernel(const float* __restrict__ src, int64_t rows, int K,
                                                      int64_t s_row, int64_t s_k, int64_t s_batch,
                                                      __nv_bfloat16* __restrict__ p0, __nv_bfloat16* __restrict__ p1,
-                                                     __nv_bfloat16* __restrict__ p2) {
+                                                     __nv_bfloat16* __restrict__ p2, int64_t ld) {
     __shared__ float tile[32][33];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
@@ -473,14 +473,15 @@ __global__ void __launch_bounds__(256) split3_kernel(const float* __restrict__ s
         const float e1 = x - __bfloat162float(x1);
         const __nv_bfloat16 x2 = __float2bfloat16_rn(e1);
         const __nv_bfloat16 x3 = __float2bfloat16_rn(e1 - __bfloat162float(x2));
-        const int64_t o = (static_cast<int64_t>(b) * rows + r) * kp + k0 + tx;
+        const int64_t o = (static_cast<int64_t>(b) * rows + r) * ld + k0 + tx;
         p0[o] = x1;
         p1[o] = x2;
         p2[o] = x3;
     }
 }
 
-bool encode_parts(CUtensorMap* m, const void* base, int64_t rows, int batch, int kp, uint32_t box_rows,
+// kp columns of rows `ld` elements apart (systems rows * ld apart)
+bool encode_parts(CUtensorMap* m, const void* base, int64_t rows, int batch, int kp, int64_t ld, uint32_t box_rows,
                   std::string* why) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) {
@@ -488,7 +489,7 @@ bool encode_parts(CUtensorMap* m, const void* base, int64_t rows, int batch, int
         return false;
     }
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kp), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(batch)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kp) * 2, static_cast<cuuint64_t>(rows) * kp * 2};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(rows) * ld * 2};
     cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -504,12 +505,20 @@ bool encode_parts(CUtensorMap* m, const void* base, int64_t rows, int batch, int
 cudaError_t split3(const TcOperand& o, int K, int kp, int batch, __nv_bfloat16* dst, cudaStream_t s) {
     const int64_t part = static_cast<int64_t>(batch) * o.rows * kp;
     dim3 grid(static_cast<unsigned>((o.rows + 31) / 32), static_cast<unsigned>(kp / 32), static_cast<unsigned>(batch));
-    split3_kernel<<<grid, 256, 0, s>>>(o.src, o.rows, K, kp, o.s_row, o.s_k, o.s_batch, dst, dst + part,
-                                       dst + 2 * part);
+    split3_kernel<<<grid, 256, 0, s>>>(o.src, o.rows, K, o.s_row, o.s_k, o.s_batch, dst, dst + part, dst + 2 * part,
+                                       kp);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t tc_split_into(const TcOperand& o, int K, int batch, const TcPreSplit& dst, cudaStream_t s) {
+    if (K < 1 || K > BK) return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>((o.rows + 31) / 32), static_cast<unsigned>(BK / 32), static_cast<unsigned>(batch));
+    split3_kernel<<<grid, 256, 0, s>>>(o.src, o.rows, K, o.s_row, o.s_k, o.s_batch, dst.base, dst.base + dst.part,
+                                       dst.base + 2 * dst.part, dst.ld);
+    return cudaGetLastError();
+}
 
 size_t tc_update_ws_bytes(int64_t rows_a, int64_t rows_b, int batch) {
     return 3ull * static_cast<size_t>(batch) * static_cast<size_t>(rows_a + rows_b) * KMAX * 2 + 1024;
@@ -524,8 +533,8 @@ bool tc_update_supported(const TcSolve* tc, int64_t M, int64_t N, int K, const f
 
 cudaError_t launch_tc_update(const TcSolve& tc, const TcOperand& A, const TcOperand* B, int K, float* C, int64_t ldc,
                              int64_t strideC, float alpha, float beta, bool lower, int batch, cudaStream_t s,
-                             std::string* why) {
-    const int64_t rows_b = B ? B->rows : 0;
+                             std::string* why, const TcPreSplit* pre_b) {
+    const int64_t rows_b = B && !pre_b ? B->rows : 0;
     if (tc_update_ws_bytes(A.rows, rows_b, batch) > tc.ws_bytes) {
         if (why) *why = "tensor-core update workspace too small";
         return cudaErrorInvalidValue;
@@ -534,15 +543,18 @@ cudaError_t launch_tc_update(const TcSolve& tc, const TcOperand& A, const TcOper
     __nv_bfloat16* wa = tc.ws;
     __nv_bfloat16* wb = wa + 3 * static_cast<int64_t>(batch) * A.rows * kp;
     cudaError_t e = split3(A, K, kp, batch, wa, s);
-    if (e == cudaSuccess && B) e = split3(*B, K, kp, batch, wb, s);
+    if (e == cudaSuccess && B && !pre_b) e = split3(*B, K, kp, batch, wb, s);
     if (e != cudaSuccess) return e;
     const int64_t N = B ? B->rows : A.rows;
     const __nv_bfloat16* bb = B ? wb : wa;
     Maps mp;
     for (int i = 0; i < 3; ++i) {
-        if (!encode_parts(&mp.a[i], wa + i * static_cast<int64_t>(batch) * A.rows * kp, A.rows, batch, kp, BM, why) ||
-            !encode_parts(&mp.b[i], bb + i * static_cast<int64_t>(batch) * N * kp, N, batch, kp, BN, why))
-            return cudaErrorInvalidValue;
+        const bool ok_a = encode_parts(&mp.a[i], wa + i * static_cast<int64_t>(batch) * A.rows * kp, A.rows, batch, kp,
+                                       kp, BM, why);
+        const bool ok_b = pre_b ? encode_parts(&mp.b[i], pre_b->base + i * pre_b->part, N, batch, kp, pre_b->ld, BN, why)
+                                : encode_parts(&mp.b[i], bb + i * static_cast<int64_t>(batch) * N * kp, N, batch, kp, kp,
+                                               BN, why);
+        if (!ok_a || !ok_b) return cudaErrorInvalidValue;
     }
     Params P{};
     P.C = C;

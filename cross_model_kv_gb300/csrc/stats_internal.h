@@ -126,10 +126,20 @@ struct TcSolve {
 };
 size_t tc_update_ws_bytes(int64_t rows_a, int64_t rows_b, int batch);
 bool tc_update_supported(const TcSolve* tc, int64_t M, int64_t N, int K, const float* C, int64_t ldc);
+// An operand already split into its three bf16 parts: part i of row r of batch item
+// b at base[i * part + (b * rows + r) * ld + k], k < K (16-byte aligned base, ld a
+// multiple of 8).
+struct TcPreSplit {
+    __nv_bfloat16* base;
+    int64_t part, ld;
+};
+// Split K columns of an operand into `dst` (K <= 64 columns, zero-padded to 64).
+cudaError_t tc_split_into(const TcOperand& o, int K, int batch, const TcPreSplit& dst, cudaStream_t s);
 // C[b] = alpha * A[b] B[b]^T + beta * C[b] (B == NULL: B = A); lower skips tiles above the diagonal.
+// With pre_b, B's parts are read from there (B->rows still gives its row count).
 cudaError_t launch_tc_update(const TcSolve& tc, const TcOperand& A, const TcOperand* B, int K, float* C, int64_t ldc,
                              int64_t strideC, float alpha, float beta, bool lower, int batch, cudaStream_t s,
-                             std::string* why);
+                             std::string* why, const TcPreSplit* pre_b = nullptr);
 
 // tc (may be NULL): run the large updates on the tensor cores.
 cudaError_t chol_factor_batched(float* G, int64_t ldg, int64_t strideG, int64_t n, int batch, int* numeric_flag,

@@ -31,16 +31,49 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kStaticScratchB
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // ID of the context the address belongs to
 
-// Device address of the scratch on the current device (looked up once per device).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// ID of the current context (unique for the life of the process), or false if
+// no context is current or the driver lacks the calls.
+bool current_context_id(unsigned long long* id) {
+    static std::once_flag once;
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext cur = nullptr;
+    if (!get_current || !get_id || get_current(&cur) != CUDA_SUCCESS || !cur) return false;
+    return get_id(cur, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch on the current device.  Set-up runs on the
+// first call on a device and again whenever that device's context is not the
+// one the address was taken in (after cudaDeviceReset, say), so a stale
+// address is never handed to a kernel.
 kvb_status scratch_on_device(int dev, unsigned char** out) {
     if (dev < 0 || dev >= kMaxDevices) return fail(KVB_ERR_UNSUPPORTED, "device index above 63");
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+    unsigned long long id = 0;
+    const bool known = current_context_id(&id);
+    if (!g_scratch_ptr[dev] || !known || id != g_scratch_ctx[dev]) {
         void* p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch");
         g_scratch_ptr[dev] = p;
+        // the lookup above makes the device's context current if none was
+        g_scratch_ctx[dev] = current_context_id(&id) ? id : 0;
     }
     *out = static_cast<unsigned char*>(g_scratch_ptr[dev]);
     return KVB_OK;

@@ -8,7 +8,6 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
-#include <cstring>
 #include <vector>
 
 #include "fit_internal.h"
@@ -68,13 +67,21 @@ namespace {
 // Bytes of solve workspace per batch of systems: half the free device memory,
 // between 4 and 48 GiB (more systems per batch keep more SMs busy in the
 // panel steps of the factorisations, which work one diagonal block at a time).
+// KVB_FIT_WORKSPACE_MB lowers the cap (a caller sharing the device, or a test
+// that wants the systems split over several batches); a batch always holds at
+// least one system.
 size_t ws_budget() {
     size_t free_b = 0, total_b = 0;
     if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
         cudaGetLastError();
         free_b = 0;
     }
-    return std::max<size_t>(size_t(4) << 30, std::min<size_t>(size_t(48) << 30, free_b / 2));
+    size_t budget = std::max<size_t>(size_t(4) << 30, std::min<size_t>(size_t(48) << 30, free_b / 2));
+    if (const char* cap = std::getenv("KVB_FIT_WORKSPACE_MB")) {
+        const long long mb = std::atoll(cap);
+        if (mb > 0) budget = std::min<size_t>(budget, static_cast<size_t>(mb) << 20);
+    }
+    return budget;
 }
 
 kvb_status st_alloc(kvb_stats* st, void** p, size_t bytes) {
@@ -485,6 +492,7 @@ kvb_status kvb_layer_select(kvb_ctx* c, kvb_stats* st, double lambda, int32_t* s
     {
         ProfScope ps(c, cs, "r2_single_source");
         for (int s0 = 0; s0 < n_sys && e == cudaSuccess; s0 += B) {
+            ProfScope pb(c, cs, "r2_solve_batch");
             const int nb = std::min(B, n_sys - s0);
             // the batch's systems of one cache at a time (system i: kv i / L_s, source
             // layer i % L_s), at most MAX_SYS per launch of the per-system kernels
@@ -589,6 +597,7 @@ kvb_status kvb_ridge_solve(kvb_ctx* c, kvb_stats* st, const int32_t* sel_k_host,
     {
         ProfScope ps(c, cs, "ridge_solve");
         for (int s0 = 0; s0 < n_sys && e == cudaSuccess; s0 += B) {
+            ProfScope pb(c, cs, "ridge_solve_batch");
             const int nb = std::min(B, n_sys - s0);
             // the batch's systems of one cache at a time (system i: kv i / nt, target
             // layer t0 + i % nt), at most MAX_SYS per launch of the per-system kernels

@@ -47,7 +47,11 @@
  * by kvb_ctx_check() and by the next call on that context.
  *
  * Environment: KVB_WAIT_TIMEOUT_MS (default 2000) bounds every device-side
- * wait, read when a context is created.  KVB_MAP_PAIR=0, KVB_MAP_PAIR_STATIC=1,
+ * wait, read when a context is created (kvb_map_apply_noalloc, which has no
+ * context, reads it on every call).  KVB_FIT_WORKSPACE_MB, read on every
+ * call, caps the solver workspace of kvb_layer_select and kvb_ridge_solve
+ * (default: half the free device memory, between 4 and 48 GiB); under a lower
+ * cap the systems are factored in more, smaller batches.  KVB_MAP_PAIR=0, KVB_MAP_PAIR_STATIC=1,
  * KVB_MAP_FUSED_STRIP=0, KVB_STATS_PAIR=0, KVB_SOLVE_PERSIST=0 and
  * KVB_STATS_TC_F32=0 select the slower comparison kernels (single-CTA map,
  * fixed tile-per-pair map, separate strip pass, single-CTA statistics,
@@ -176,10 +180,12 @@ kvb_status kvb_map_apply(kvb_ctx* ctx, kvb_dtype dtype, const void* src_k, const
  *   alignment) must fit in 64 MiB, else KVB_ERR_INVALID_ARG; e.g. about 800
  *   tokens at the Qwen3-14B -> 32B shape with max_pos = T.
  *   The first call on each device looks up the array's device address with
- *   cudaGetSymbolAddress; make that first call before capturing a stream.
+ *   cudaGetSymbolAddress (again after that device's context is re-created,
+ *   e.g. by cudaDeviceReset); make that first call before capturing a stream.
  *   Every call reuses the same array, so calls that overlap on the GPU (other
  *   streams, other host threads) race: serialise them.  The call waits for its
  *   own kernels on `stream` and returns their errors (bad position, timeout).
+ *   It reads KVB_WAIT_TIMEOUT_MS on every call.
  */
 kvb_status kvb_map_apply_noalloc(const kvb_model_spec* src, const kvb_model_spec* tgt, int32_t top_k,
                                  int32_t max_pos, const void* src_k, const void* src_v,

@@ -20,7 +20,10 @@ FineWeb-Edu calibration text are not available, these stand in for them):
 * noise draws are standard normal; the consumer scales them (sigma = 1e-3, or
   per column to a signal-to-noise ratio);
 * ragged batches: lengths uniform in [lo, hi], positions restart at 0 per
-  sequence, sequences packed along the token axis.
+  sequence, sequences packed along the token axis;
+* correlated layers (full-size solver checks): every layer of a cache is
+  s_ch * (rho * z + sqrt(1 - rho^2) * e_l) with one shared draw z, so the
+  channel marginals are unchanged and layers correlate by rho^2.
 """
 from .generators import (  # noqa: F401
     channel_scales,
@@ -31,5 +34,6 @@ from .generators import (  # noqa: F401
     ragged_lengths,
     packed_positions,
     torch_content,
+    torch_content_shared,
     torch_weights,
 )

@@ -77,6 +77,26 @@ def torch_content(seed, L: int, H: int, T: int, d: int, sigma: float, dtype, dev
     return out
 
 
+def torch_content_shared(seed, L: int, H: int, T: int, d: int, sigma: float, rho: float, dtype, device):
+    """Content [L][H][T][d] whose layers share one component: for every layer,
+    s_ch * (rho * z + sqrt(1 - rho^2) * e_l), z and e_l standard normal, z the
+    same draw [H][T][d] for every layer.  Each channel is N(0, s_ch^2) as in
+    `content`; two layers correlate by rho^2 channel by channel (the layers of
+    one model's cache are correlated through its residual stream)."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out = torch.empty((L, H, T, d), dtype=dtype, device=device)
+    s = torch.exp(sigma * torch.randn((L, H, 1, d), generator=g, device=device, dtype=torch.float32))
+    z = torch.randn((H, T, d), generator=g, device=device, dtype=torch.float32)
+    a, b = float(rho), float(np.sqrt(1.0 - rho * rho))
+    for l in range(L):
+        x = torch.randn((H, T, d), generator=g, device=device, dtype=torch.float32)
+        out[l].copy_((a * z + b * x) * s[l])
+    return out
+
+
 def torch_weights(seed, L_tgt: int, p: int, q: int, dtype, device, bias_std: float = 0.1,
                   out_major: bool = True):
     """Hidden weights on `device`.

@@ -260,7 +260,7 @@ def test_bf16_tensor_core_statistics_head_dims_packed_short_sequences(kvb, d, H)
 def test_target_layer_blocks_reproduce_the_full_fit(kvb, dtype, d):
     # statistics of a target-layer block hold only that block's target columns;
     # one calibration pass per block gives the selections, R^2 and maps of the
-    # object that holds every target layer
+    # object that holds every target layer, and of the float64 oracle
     # 8 sequences x 512 tokens, stride 4: 1024 observations for 2 x 2 x d features
     pair = make_pair(31, 4, 5, 2, d, 2, 512, 8, 1e4, 1e6, noise=1e-2, sigma=1.0)
     if dtype == torch.bfloat16:
@@ -290,6 +290,19 @@ def test_target_layer_blocks_reproduce_the_full_fit(kvb, dtype, d):
     assert np.abs(to_host64(br2) - r2).max() <= 1e-5
     for a, b in ((bWk, Wk), (bWv, Wv), (bbk, bk), (bbv, bv)):
         assert rel_fro(to_host64(a), to_host64(b)) <= 1e-5
+    # the blocked fit against the float64 oracle (KVBridge "Loading": blocking changes
+    # how many passes the fit takes, not what it computes)
+    fit = O.fit_mapper(pair["calib"], pair["theta_s"], pair["theta_t"], k, 0.01, 4)
+    assert np.array_equal(bsk, fit.sel_k) and np.array_equal(bsv, fit.sel_v)
+    assert np.array_equal(fit.sel_k, pair["sel_k"]) and np.array_equal(fit.sel_v, pair["sel_v"])
+    br2h = to_host64(br2)
+    assert np.max(np.abs(br2h[0] - fit.r2_k)) < 1e-4 and np.max(np.abs(br2h[1] - fit.r2_v)) < 1e-4
+    w_tol = TOL_W if dtype == torch.bfloat16 else 1e-4
+    for gw, ow in ((bWk, fit.W_k), (bWv, fit.W_v)):
+        e = rel_fro(np.transpose(to_host64(gw), (0, 2, 1)), ow)
+        assert e <= w_tol, e
+    for gb, ob in ((bbk, fit.b_k), (bbv, fit.b_v)):
+        assert rel_fro(to_host64(gb), ob) <= w_tol
 
 
 def test_target_block_range_is_validated(kvb):
@@ -318,97 +331,6 @@ def test_bf16_fit_cuda_core_statistics_path(kvb):
     _accumulate(kvb, ctx, st, pair["calib"], torch.bfloat16)
     _check_stats(kvb, st, pair, 1e-5)
     _check_fit(kvb, ctx, st, pair, torch.bfloat16, 5e-3)
-
-
-def test_qwen3_14b_to_32b_calibration_pass_sampled(kvb):
-    # Calibration pass at the 14B -> 32B shapes: 40 -> 64 layers, 8 KV heads, head_dim 128,
-    # k = 8, 256 sequences x 1024 tokens in 32 batches of 8192, stride 4 -> 65,536 observations.
-    # Targets are fixed mixtures of 8 hidden source layers (same RoPE theta on both sides, so
-    # content-space targets are the same mixtures) plus noise.  Checked against the oracle on
-    # sampled (layer, head) slabs of the statistics and on sampled single-source R^2 pairs;
-    # the selection must recover the hidden layers.
-    import synth
-    L_s, L_t, H, d, k, Tb, nb_, lam = 40, 64, 8, 128, 8, 8192, 32, 0.01
-    theta = 1e6
-    dev = "cuda"
-    sel_k = synth.hidden_selection(501, L_s, L_t, k)
-    sel_v = synth.hidden_selection(502, L_s, L_t, k)
-    coef = np.linspace(1.0, 0.6, k)
-    pos = torch.arange(1024, dtype=torch.int32, device=dev).repeat(Tb // 1024)
-    keep = torch.arange(0, Tb, 4, device=dev)  # pos % 4 == 0
-    ctx = kvb.kvb_ctx_create(spec(L_s, H, d, theta), spec(L_t, H, d, theta), k, 1024)
-    st = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, Tb)
-    g = torch.Generator(device=dev)
-    g.manual_seed(503)
-    src_slabs = [(0, 0), (17, 3), (39, 7)]
-    tgt_slabs = [(0, 0), (31, 5), (63, 7)]
-    t_star = 5
-    s_true_k, s_true_v = int(sel_k[t_star][0]), int(sel_v[t_star][0])
-    s_false_k = int(next(s for s in range(L_s) if s not in sel_k[t_star]))
-    s_false_v = int(next(s for s in range(L_s) if s not in sel_v[t_star]))
-    host = {key: [] for key in ("sk", "sv", "tk", "tv", "pk", "pv", "yk", "yv")}
-    hsel = lambda x: x.index_select(1, keep).to(torch.float64).cpu().numpy()  # [..][kept][d]
-    for b in range(nb_):
-        sk = synth.torch_content(600 + b, L_s, H, Tb, d, 1.0, torch.bfloat16, dev)
-        sv = synth.torch_content(700 + b, L_s, H, Tb, d, 1.0, torch.bfloat16, dev)
-        tk = torch.empty((L_t, H, Tb, d), dtype=torch.bfloat16, device=dev)
-        tv = torch.empty_like(tk)
-        for t in range(L_t):
-            for out, src, sel in ((tk, sk, sel_k), (tv, sv, sel_v)):
-                acc = 0.1 * torch.randn((H, Tb, d), generator=g, device=dev)
-                for j in range(k):
-                    acc += float(coef[j]) * src[int(sel[t][j])].float()
-                out[t].copy_(acc)
-        kvb.kvb_stats_accumulate(ctx, st, sk, sv, tk, tv, pos, 4)
-        host["sk"].append(np.stack([hsel(sk[l, h][None])[0] for l, h in src_slabs]))
-        host["sv"].append(np.stack([hsel(sv[l, h][None])[0] for l, h in src_slabs]))
-        host["tk"].append(np.stack([hsel(tk[l, h][None])[0] for l, h in tgt_slabs]))
-        host["tv"].append(np.stack([hsel(tv[l, h][None])[0] for l, h in tgt_slabs]))
-        host["pk"].append(np.stack([hsel(sk[s]) for s in (s_true_k, s_false_k)]))
-        host["pv"].append(np.stack([hsel(sv[s]) for s in (s_true_v, s_false_v)]))
-        host["yk"].append(hsel(tk[t_star]))
-        host["yv"].append(hsel(tv[t_star]))
-        del sk, sv, tk, tv
-    kvb.kvb_ctx_check(ctx)
-    assert kvb.kvb_stats_count(st) == 65536
-    pos_kept = np.tile(np.arange(0, 1024, 4), nb_ * (Tb // 1024))
-    cat = {key: np.concatenate(v, axis=-2) for key, v in host.items()}  # observations on axis -2
-
-    def slab_features(arr, slabs, strip_theta):
-        cols = []
-        for i in range(len(slabs)):
-            x = arr[i]  # [N][d]
-            if strip_theta is not None:
-                x = O.strip(x, pos_kept, strip_theta)
-            cols.append(x)
-        return np.concatenate(cols, axis=1)
-
-    q, Fs, Ft = H * d, L_s * H * d, L_t * H * d
-    f_src = np.concatenate([np.arange((l * H + h) * d, (l * H + h + 1) * d) for l, h in src_slabs])
-    f_tgt = np.concatenate([np.arange((l * H + h) * d, (l * H + h + 1) * d) for l, h in tgt_slabs])
-    r2 = torch.empty((2, L_t, L_s), dtype=torch.float32, device=dev)
-    for kv, (xs, ys) in enumerate((("sk", "tk"), ("sv", "tv"))):
-        th = theta if kv == 0 else None
-        ref = O.centered_stats(slab_features(cat[xs], src_slabs, th), slab_features(cat[ys], tgt_slabs, th))
-        n, mx, my, gram, cross, syy = _export(kvb, st, kv, Fs, Ft)
-        scale_m = np.sqrt(np.outer(np.diag(ref.M), np.diag(ref.M)))
-        assert np.max(np.abs(gram[np.ix_(f_src, f_src)] - ref.M) / scale_m) < 1e-4
-        scale_c = np.sqrt(np.outer(np.diag(ref.M), ref.syy))
-        assert np.max(np.abs(cross[np.ix_(f_src, f_tgt)] - ref.C) / scale_c) < 1e-4
-        assert rel_fro(syy[f_tgt], ref.syy) < 1e-4
-        assert np.max(np.abs(mx[f_src] - ref.xbar)) < 1e-4 and np.max(np.abs(my[f_tgt] - ref.ybar)) < 1e-4
-    gk, gv = kvb.kvb_layer_select(ctx, st, lam, r2)
-    assert np.array_equal(gk, sel_k) and np.array_equal(gv, sel_v)
-    r2h = to_host64(r2)
-    for kv, (px, yy, pair) in enumerate((("pk", "yk", (s_true_k, s_false_k)), ("pv", "yv", (s_true_v, s_false_v)))):
-        th = theta if kv == 0 else None
-        feats = lambda a: O.strip(a, pos_kept, th) if th else a
-        Xs = [np.transpose(feats(cat[px][i]), (1, 0, 2)).reshape(-1, q) for i in range(2)]
-        Y = np.transpose(feats(cat[yy]), (1, 0, 2)).reshape(-1, q)
-        ref = O.single_source_r2(Xs, [Y], lam, H, d)[0]
-        got = np.array([r2h[kv, t_star, pair[0]], r2h[kv, t_star, pair[1]]])
-        assert np.max(np.abs(got - ref)) < 1e-4, (got, ref)
-        assert ref[0] > ref[1] + 0.02
 
 
 def test_no_observations_and_zero_lambda_is_a_numeric_error(kvb):

@@ -1,16 +1,24 @@
 """kvb_map_apply_noalloc: the mapper apply for callers that may not allocate
-device memory (code living inside another framework's memory pool, or a
-runtime that owns the whole device budget).  It keeps its scratch in a fixed
-array of the library; its results must match kvb_map_apply's.
+device memory at all -- code running inside another framework's memory pool
+(which owns every byte of the device), or a runtime that hands the library a
+fixed budget up front.  Such callers cannot create a context, so this entry
+point keeps its scratch in a fixed array inside the library instead.
+
+Its results must be the same bits as kvb_map_apply's (both run the same strip
+and map kernels; the separate strip pass and the one fused into the map kernel
+are bit-identical), agree with the float64 oracle, leave the device's free
+memory unchanged, and report a bad position through the status it returns.
 
 This file is collected last on purpose, so a run that stops at the first
 failure has already run every other test."""
 import numpy as np
 import pytest
 
-from cases import TOL_BF16, ApplyCase, rel_fro, spec, to_host64
+from cases import TOL_BF16, ApplyCase, rel_fro, spec
 
 torch = pytest.importorskip("torch")
+
+MAX_POS = 600
 
 
 @pytest.fixture(scope="module")
@@ -21,32 +29,73 @@ def kvb():
     return m
 
 
-def _noalloc(kvb, c, max_pos, out_k, out_v):
-    kvb.kvb_map_apply_noalloc(spec(c.L_s, c.H, c.d, c.theta_s), spec(c.L_t, c.H, c.d, c.theta_t), c.k, max_pos,
-                              c.src_k, c.src_v, c.positions, c.sel_k, c.sel_v, c.W_k, c.W_v, c.b_k, c.b_v,
-                              out_k, out_v)
+def _noalloc(kvb, c, out_k, out_v, positions=None):
+    kvb.kvb_map_apply_noalloc(spec(c.L_s, c.H, c.d, c.theta_s), spec(c.L_t, c.H, c.d, c.theta_t), c.k, MAX_POS,
+                              c.src_k, c.src_v, c.positions if positions is None else positions, c.sel_k, c.sel_v,
+                              c.W_k, c.W_v, c.b_k, c.b_v, out_k, out_v)
+
+
+def _cases():
+    rng = np.random.default_rng(41)
+    pos_b = rng.integers(0, MAX_POS, size=500).astype(np.int32)
+    return [ApplyCase(6, 4, 8, 128, 3, 500, 1e4, 1e6, torch.bfloat16, seed=40),
+            ApplyCase(6, 4, 8, 128, 3, 500, 1e4, 1e6, torch.bfloat16, seed=80, positions=pos_b)]
 
 
 @pytest.mark.gpu
 def test_noalloc_matches_the_context_entry_point_on_two_calls_in_a_row(kvb):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    rng = np.random.default_rng(41)
-    pos_b = rng.integers(0, 600, size=500).astype(np.int32)
-    cases = [ApplyCase(6, 4, 8, 128, 3, 500, 1e4, 1e6, torch.bfloat16, seed=40),
-             ApplyCase(6, 4, 8, 128, 3, 500, 1e4, 1e6, torch.bfloat16, seed=80, positions=pos_b)]
-    for c in cases:  # two different inputs, one call each, back to back
-        ctx = kvb.kvb_ctx_create(spec(c.L_s, c.H, c.d, c.theta_s), spec(c.L_t, c.H, c.d, c.theta_t), c.k, 600)
+    cases = _cases()
+    refs = []
+    for c in cases:
+        ctx = kvb.kvb_ctx_create(spec(c.L_s, c.H, c.d, c.theta_s), spec(c.L_t, c.H, c.d, c.theta_t), c.k, MAX_POS)
         c.run(kvb, ctx)
         kvb.kvb_ctx_check(ctx)
-        ref_k, ref_v = to_host64(c.out_k), to_host64(c.out_v)
-        out_k = torch.full_like(c.out_k, float("nan"))
-        out_v = torch.full_like(c.out_v, float("nan"))
-        _noalloc(kvb, c, 600, out_k, out_v)
-        torch.cuda.synchronize()
-        ek, ev = rel_fro(to_host64(out_k), ref_k), rel_fro(to_host64(out_v), ref_v)
-        assert ek <= TOL_BF16 and ev <= TOL_BF16, (ek, ev)
+        refs.append((c.out_k.clone(), c.out_v.clone()))
         kvb.kvb_ctx_destroy(ctx)
+    outs = [(torch.full_like(c.out_k, float("nan")), torch.full_like(c.out_v, float("nan"))) for c in cases]
+    # first call on this device: sets up the scratch address (and loads the kernels' modules)
+    _noalloc(kvb, cases[0], *outs[0])
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    for c, (ok, ov) in zip(cases, outs):  # two different inputs, back to back
+        ok.fill_(float("nan"))
+        ov.fill_(float("nan"))
+        _noalloc(kvb, c, ok, ov)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    rng = np.random.default_rng(7)
+    for c, (ok, ov), (rk, rv) in zip(cases, outs, refs):
+        assert torch.equal(ok, rk) and torch.equal(ov, rv)
+        layers = np.array([0, c.L_t - 1])
+        tokens = np.sort(rng.choice(c.T, size=96, replace=False))
+        ek_o, ev_o = c.oracle(layers, tokens)
+        c.out_k, c.out_v = ok, ov
+        gk, gv = c.gpu(layers, tokens)
+        ek, ev = rel_fro(gk, ek_o), rel_fro(gv, ev_o)
+        assert ek <= TOL_BF16 and ev <= TOL_BF16, (ek, ev)
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_a_position_beyond_max_pos(kvb):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    c = _cases()[0]
+    bad = c.positions.clone()
+    bad[123] = MAX_POS  # one position outside [0, max_pos): its rows become zeros, the call reports it
+    ok, ov = torch.empty_like(c.out_k), torch.empty_like(c.out_v)
+    with pytest.raises(kvb.KvbError) as e:
+        _noalloc(kvb, c, ok, ov, positions=bad)
+    assert e.value.status == 1
+    assert torch.count_nonzero(ok[:, :, 123]) == 0
+    # the error word is cleared by the next call, which maps correctly again
+    _noalloc(kvb, c, ok, ov)
+    torch.cuda.synchronize()
+    rk, rv = c.oracle(np.array([1]), np.arange(0, c.T, 7))
+    c.out_k, c.out_v = ok, ov
+    gk, gv = c.gpu(np.array([1]), np.arange(0, c.T, 7))
+    assert rel_fro(gk, rk) <= TOL_BF16 and rel_fro(gv, rv) <= TOL_BF16
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(kvb):

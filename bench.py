@@ -301,11 +301,16 @@ def run_fit(kvb, dev, seed=101, small=False, block=0, f32=False):
     gemm_name = "stats_gemm_tcgen05" if "stats_gemm_tcgen05" in kern else "stats_gemm_simt"
     gemm_n, gemm_ms = kern.get(gemm_name, (0, 0.0))
     gather_n, gather_ms = kern.get("calib_gather_center", (0, 0.0))
+    gather_ms += kern.get("calib_first_mean", (0, 0.0))[1]  # the first batch's mean pre-pass
     nb = Tb // F["stride"]
-    # algorithmic bytes: kept rows of the four caches read once, centered (hi, lo) operands written once
+    # algorithmic bytes: kept rows of the four caches read once, centered (hi, lo) operands written
+    # once; the first 128 kept rows of every pass's first batch are read once more for the shift
+    blk = max(t1 - t0 for t0, t1 in blocks)
+    per_batch_rows = (2 * L_s * H + 2 * blk * H) * min(nb, 128) * d * 2
     gather_bytes = n_batches * (len(blocks) * (2 * L_s * H * nb * d * 2 + 2 * Fs * nb * 4) +
                                 2 * L_t * H * nb * d * 2 + 2 * Ft * nb * 4)
-    blk = max(t1 - t0 for t0, t1 in blocks)
+    if not f32:
+        gather_bytes += len(blocks) * per_batch_rows
     out = {"workload": (f"{L_s}->{L_t} layers, k={k}, " if small else "qwen3-14b->32b-shaped fit: ") +
                        f"{F['n_seq']} x {F['seq_len']} calibration tokens in {n_batches} batches of {Tb}, stride 4, "
                        + ("fp32 caches, fp32 statistics (three-part bf16 tensor-core products), lambda 0.01" if f32 else

@@ -260,17 +260,12 @@ __global__ void __launch_bounds__(256, (R <= 4 ? 2 : 1)) gather_shift_kernel(con
     const __nv_bfloat16* base = cache + static_cast<int64_t>(slab) * T_len * d;
     const int64_t f0 = static_cast<int64_t>(slab) * d;
 
-    float slo[8], shi[8];
-    if (*n_seen > 0) {
+    float slo[8], shi[8];  // shift: the running mean (on the first batch, the batch mean)
+    (void)n_seen;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            slo[i] = mean_a[f0 + 8 * l + i];
-            shi[i] = mean_a[f0 + half + 8 * l + i];
-        }
-    } else {  // first batch: shift by the first kept row (n >= 1 here)
-        const int tok = __ldg(rows);
-        pair8(base + static_cast<int64_t>(tok) * d, l, half, strip, tab + static_cast<int64_t>(__ldg(pos + tok)) * half,
-              slo, shi);
+    for (int i = 0; i < 8; ++i) {
+        slo[i] = mean_a[f0 + 8 * l + i];
+        shi[i] = mean_a[f0 + half + 8 * l + i];
     }
     if (blockIdx.x == 0 && rq == 0) {
 #pragma unroll
@@ -450,7 +445,7 @@ __global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(con
     const int n = *nb;
     const int i = threadIdx.x % HALF;  // RoPE pair (i, i + D/2)
     const int q = threadIdx.x / HALF;  // rows q*ROWS .. q*ROWS + ROWS - 1 of the chunk
-    const bool first_batch = *n_seen == 0;
+    (void)n_seen;  // shift: the running mean (on the first batch, the batch mean)
 
     // work items (chunk, slab) in chunk-major order; CTA b takes one contiguous
     // range of them, i.e. runs of slabs within one or two chunks
@@ -484,7 +479,7 @@ __global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(con
             const int slab = s_begin + j;
             const __nv_bfloat16* base = cache + static_cast<int64_t>(slab) * T_len * D;
             __nv_bfloat16* dst = stg + static_cast<size_t>(j % kStages) * kChunk * D;
-            if (!first_batch && threadIdx.x < D / 4)
+            if (threadIdx.x < D / 4)
                 cp_async16(smean + (j % kStages) * D + 4 * threadIdx.x, mean_a + static_cast<int64_t>(slab) * D +
                            4 * threadIdx.x, 16);
             for (int pc = threadIdx.x; pc < PIECES; pc += blockDim.x) {
@@ -523,23 +518,8 @@ __global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(con
             const int slab = s_begin + j;
             const int64_t f0 = static_cast<int64_t>(slab) * D;
             const __nv_bfloat16* raw = stg + static_cast<size_t>(j % kStages) * kChunk * D;
-            float sl, sh;  // shift of features i and i + D/2
-            if (!first_batch) {
-                sl = smean[(j % kStages) * D + i];
-                sh = smean[(j % kStages) * D + HALF + i];
-            } else {  // first batch: shift by the first kept row (n >= 1 here)
-                const int tok = __ldg(rows);
-                const __nv_bfloat16* row0 = cache + static_cast<int64_t>(slab) * T_len * D + static_cast<int64_t>(tok) * D;
-                const float x = __bfloat162float(row0[i]), y = __bfloat162float(row0[HALF + i]);
-                if (strip) {
-                    const float2 cs = __ldg(tab + static_cast<int64_t>(__ldg(pos + tok)) * HALF + i);
-                    sl = fmaf(x, cs.x, y * cs.y);
-                    sh = fmaf(y, cs.x, -(x * cs.y));
-                } else {
-                    sl = x;
-                    sh = y;
-                }
-            }
+            const float sl = smean[(j % kStages) * D + i];  // shift of features i and i + D/2
+            const float sh = smean[(j % kStages) * D + HALF + i];
             if (chunk == 0 && q == 0) {
                 shift_out[f0 + i] = sl;
                 shift_out[f0 + HALF + i] = sh;
@@ -596,6 +576,58 @@ __global__ void __launch_bounds__(stream_threads(D), 1) gather_stream_kernel(con
     }
 }
 
+// First batch of a fit (nothing merged yet): the column means of the batch's
+// first 128 kept rows (keys stripped) become the running means before the
+// single-pass gather, which shifts every value by the running mean.  Later
+// batches return at once.  A shift near the batch mean (within ~sigma / 11
+// here) keeps every centered sum near its final size; a shift far from it (one
+// row, say) leaves sums of order n * shift^2 that cancel in the merge and cost
+// the fp32 accumulation its precision.  Grid (slab, matrix), 256 threads:
+// thread (pair i, row group g) sums rows g, g + G, ... of its slab.
+constexpr int kFirstRows = 128;
+
+__global__ void __launch_bounds__(256) first_mean_kernel(FirstMeanArgs a) {
+    if (*a.n_seen != 0) return;
+    const int n = *a.nb < kFirstRows ? *a.nb : kFirstRows;
+    const int m = blockIdx.y;
+    const int64_t slab = blockIdx.x;
+    if (n == 0 || slab >= a.n_slabs[m]) return;
+    const int half = a.d >> 1;
+    const int G = 256 / half;
+    const int i = threadIdx.x % half, g = threadIdx.x / half;
+    const __nv_bfloat16* base = a.cache[m] + slab * a.T * a.d;
+    const float2* tab = a.tab[m];
+    float sa = 0.f, sb = 0.f;
+    if (g < G) {
+        for (int r = g; r < n; r += G) {
+            const int tok = __ldg(a.rows + r);
+            const __nv_bfloat16* row = base + static_cast<int64_t>(tok) * a.d;
+            const float x = __bfloat162float(row[i]), y = __bfloat162float(row[half + i]);
+            if (tab) {
+                const float2 cs = __ldg(tab + static_cast<int64_t>(__ldg(a.pos + tok)) * half + i);
+                sa += fmaf(x, cs.x, y * cs.y);
+                sb += fmaf(y, cs.x, -(x * cs.y));
+            } else {
+                sa += x;
+                sb += y;
+            }
+        }
+    }
+    __shared__ float red[2][256];
+    red[0][threadIdx.x] = sa;
+    red[1][threadIdx.x] = sb;
+    __syncthreads();
+    if (threadIdx.x < half) {
+        float ta = 0.f, tb = 0.f;
+        for (int k = 0; k < G; ++k) {
+            ta += red[0][k * half + threadIdx.x];
+            tb += red[1][k * half + threadIdx.x];
+        }
+        a.mean[m][slab * a.d + threadIdx.x] = ta / static_cast<float>(n);
+        a.mean[m][slab * a.d + half + threadIdx.x] = tb / static_cast<float>(n);
+    }
+}
+
 // zsum[c] = sum over the batch's chunks of part[chunk][c].
 __global__ void zsum_kernel(const float* __restrict__ part, int64_t F, const int* __restrict__ nb,
                             float* __restrict__ zsum) {
@@ -619,11 +651,18 @@ __global__ void chan_prepare_kernel(MeanSet ms, const long long* __restrict__ n_
         coef[0] = n > 0 ? static_cast<float>(static_cast<double>(na) * n_b / n) : 0.f;
         coef[1] = static_cast<float>(n_b);
     }
+    const float f = n > 0 ? static_cast<float>(static_cast<double>(na) * n_b / n) : 0.f;
+    const int chunks = (n_b + kChunk - 1) / kChunk;
     for (int m = 0; m < 4; ++m) {
         for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < ms.len[m];
              c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
             float zbar = 0.f, xb;
-            if (ms.zsum[m]) {
+            if (ms.part) {
+                float zs = 0.f;
+                for (int k = 0; k < chunks; ++k) zs += ms.part[k * ms.Fall + ms.foff[m] + c];
+                zbar = n_b > 0 ? zs / static_cast<float>(n_b) : 0.f;
+                xb = ms.shift[m][c] + zbar;
+            } else if (ms.zsum[m]) {
                 zbar = n_b > 0 ? ms.zsum[m][c] / static_cast<float>(n_b) : 0.f;
                 xb = ms.shift[m][c] + zbar;
             } else {
@@ -633,6 +672,11 @@ __global__ void chan_prepare_kernel(MeanSet ms, const long long* __restrict__ n_
             ms.delta[m][c] = dl;
             ms.zbar[m][c] = zbar;
             ms.mean[m][c] += dl * wb;
+            if (ms.part && m >= 2) {  // S_yy += sum z^2 - g zbar^2 + f delta^2
+                float sq = 0.f;
+                for (int k = 0; k < chunks; ++k) sq += ms.part_sq[k * ms.Fsq + ms.qoff[m] + c];
+                ms.syy[m - 2][c] += sq - static_cast<float>(n_b) * zbar * zbar + f * dl * dl;
+            }
         }
     }
 }
@@ -824,6 +868,14 @@ cudaError_t launch_gather(const GatherArgs& g, cudaStream_t s) {
             static_cast<const __nv_bfloat16*>(g.cache), g.T, g.d, g.rows, g.nb, g.pos, g.tab, g.strip, g.bmean, g.out,
             g.out_lo, g.out_3, g.ld);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_first_mean(const FirstMeanArgs& a, cudaStream_t s) {
+    int64_t most = 0;
+    for (int m = 0; m < 4; ++m) most = a.n_slabs[m] > most ? a.n_slabs[m] : most;
+    if (most == 0) return cudaSuccess;
+    first_mean_kernel<<<dim3(static_cast<unsigned>(most), 4), 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -32,6 +32,10 @@ struct kvb_stats {
     float* zsum[4] = {};   // column sums of the shifted batch (single-pass gather)
     float* shift[4] = {};  // shift of the batch (single-pass gather)
     float* part = nullptr; // [ld/64][max(Fs, Ft)] per-chunk column sums of one matrix
+    // four-matrix gather (bf16, head_dim 128): per-chunk column sums of all four
+    // matrices [ld/128][2 Fs + 2 Ft] and target sums of squares [ld/128][2 Ft]
+    float* part_all = nullptr;
+    float* part_sq = nullptr;
     float* gram[2] = {};   // [Fs][Fs], lower triangle kept
     float* cross[2] = {};  // [Fs][Ft]
     float* syy[2] = {};    // [Ft]
@@ -262,6 +266,12 @@ kvb_status kvb_stats_create_block(kvb_ctx* ctx, kvb_dtype dtype, int64_t max_bat
         }
     }
     A(reinterpret_cast<void**>(&st->part), static_cast<size_t>(st->ld / 128) * std::max(st->Fs, st->Ft) * 4);
+    // one gather launch for all four matrices unless KVB_GATHER_ALL=0 (one launch per matrix)
+    const char* gall = std::getenv("KVB_GATHER_ALL");
+    if (st->use_tc && gather_all_supported(dtype, ctx->d) && !(gall && std::strcmp(gall, "0") == 0)) {
+        A(reinterpret_cast<void**>(&st->part_all), static_cast<size_t>(st->ld / 128) * 2 * (st->Fs + st->Ft) * 4);
+        A(reinterpret_cast<void**>(&st->part_sq), static_cast<size_t>(st->ld / 128) * 2 * st->Ft * 4);
+    }
     A(reinterpret_cast<void**>(&st->r2), 2ull * ctx->L_t * ctx->L_s * 4);
     A(reinterpret_cast<void**>(&st->sel), 2ull * ctx->L_t * ctx->k * 4);
     if (s == KVB_OK) s = zero_stats(st, 0);
@@ -332,10 +342,60 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
         e = launch_select_rows(positions, T, stride, c->max_pos, st->rows, st->nb_dev, err, cs);
     }
     if (e != cudaSuccess) return cuda_fail(e, "row selection");
+    const bool fused = st->part_all != nullptr;  // one launch for the four matrices, S_yy in the merge
+    const bool single = gather_single_pass_ok(dt, c->d);
+    if (single) {  // the first batch's own means become the shift (returns at once on later batches)
+        ProfScope ps(c, cs, "calib_first_mean");
+        FirstMeanArgs fm{};
+        for (int m = 0; m < 4; ++m) {
+            fm.cache[m] = static_cast<const __nv_bfloat16*>(caches[m]);
+            fm.n_slabs[m] = slabs[m];
+            fm.tab[m] = tabs[m];
+            fm.mean[m] = st->mean[m];
+        }
+        fm.T = T;
+        fm.d = c->d;
+        fm.rows = st->rows;
+        fm.nb = st->nb_dev;
+        fm.n_seen = st->n_dev;
+        fm.pos = positions;
+        e = launch_first_mean(fm, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "first-batch means");
+    }
     {
         ProfScope ps(c, cs, "calib_gather_center");
-        const bool single = gather_single_pass_ok(dt, c->d);
-        for (int m = 0; m < 4 && e == cudaSuccess; ++m) {
+        if (fused) {
+            GatherAllArgs ga{};
+            int64_t fo = 0, qo = 0;
+            for (int m = 0; m < 4; ++m) {
+                ga.cache[m] = static_cast<const __nv_bfloat16*>(caches[m]);
+                ga.n_slabs[m] = slabs[m];
+                ga.foff[m] = fo;
+                fo += slabs[m] * c->d;
+                ga.qoff[m] = m >= 2 ? qo : -1;
+                if (m >= 2) qo += slabs[m] * c->d;
+                ga.tab[m] = tabs[m];
+                ga.mean_a[m] = st->mean[m];
+                ga.shift[m] = st->shift[m];
+                ga.out[m] = static_cast<__nv_bfloat16*>(outs[m]);
+                ga.out_lo[m] = static_cast<__nv_bfloat16*>(outs_lo[m]);
+            }
+            ga.T = T;
+            ga.ld = st->ld;
+            ga.Fall = fo;
+            ga.Fsq = qo;
+            ga.rows = st->rows;
+            ga.nb = st->nb_dev;
+            ga.n_seen = st->n_dev;
+            ga.pos = positions;
+            ga.part = st->part_all;
+            ga.part_sq = st->part_sq;
+            ga.err = err;
+            ga.stride = stride;
+            ga.max_pos = c->max_pos;
+            e = launch_gather_all(ga, c->num_sms, cs);
+        }
+        for (int m = 0; m < 4 && e == cudaSuccess && !fused; ++m) {
             GatherArgs g{};
             g.dt = dt;
             g.cache = caches[m];
@@ -361,7 +421,27 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
             g.ld = st->ld;
             e = launch_gather(g, cs);
         }
-        MeanSet ms;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "gather/center");
+    {
+        ProfScope ps(c, cs, "calib_chan_prepare");
+        MeanSet ms{};
+        if (fused) {
+            ms.part = st->part_all;
+            ms.part_sq = st->part_sq;
+            int64_t fo = 0, qo = 0;
+            for (int m = 0; m < 4; ++m) {
+                const int64_t w = slabs[m] * c->d;
+                ms.foff[m] = fo;
+                fo += w;
+                ms.qoff[m] = m >= 2 ? qo : -1;
+                if (m >= 2) qo += w;
+            }
+            ms.Fall = fo;
+            ms.Fsq = qo;
+            ms.syy[0] = st->syy[0];
+            ms.syy[1] = st->syy[1];
+        }
         for (int m = 0; m < 4; ++m) {
             ms.mean[m] = st->mean[m];
             ms.bmean[m] = st->bmean[m];
@@ -374,7 +454,7 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
         ms.len[2] = ms.len[3] = st->Ft;
         if (e == cudaSuccess) e = launch_chan_prepare(ms, st->n_dev, st->nb_dev, st->coef_dev, cs);
     }
-    if (e != cudaSuccess) return cuda_fail(e, "gather/center");
+    if (e != cudaSuccess) return cuda_fail(e, "Chan merge preparation");
     StatsJob jobs[4];
     stats_jobs(st, jobs);
     if (st->use_tc) {
@@ -392,7 +472,7 @@ kvb_status kvb_stats_accumulate(kvb_ctx* c, kvb_stats* st, const void* src_k, co
     if (e != cudaSuccess) return cuda_fail(e, "statistics GEMM");
     {
         ProfScope ps(c, cs, "calib_syy_merge");
-        for (int kv = 0; kv < 2 && e == cudaSuccess; ++kv)
+        for (int kv = 0; kv < 2 && e == cudaSuccess && !fused; ++kv)  // (fused: done in the merge)
             e = launch_syy(st->YT[kv], st->YT_lo[kv], st->YT_3[kv], st->ld, st->Ft, st->nb_dev, st->delta[2 + kv], st->zbar[2 + kv],
                            st->coef_dev, st->syy[kv], cs);
         if (e == cudaSuccess) e = launch_chan_finish(st->n_dev, st->nb_dev, cs);

@@ -9,6 +9,9 @@ namespace kvb {
 
 // Four running-mean vectors: source keys, source values, target keys, target values.
 // zsum/shift are set (single-pass path) or NULL (generic path, bmean used).
+// With part set (the four-matrix gather), the column sums are the per-chunk
+// partial sums part[chunk][foff[m] + c] added in chunk order, and the targets'
+// S_yy is updated here from part_sq[chunk][qoff[m] + c] (no separate pass).
 struct MeanSet {
     float* mean[4];
     const float* bmean[4];
@@ -17,7 +20,39 @@ struct MeanSet {
     float* delta[4];
     float* zbar[4];
     int64_t len[4];
+    const float* part;
+    const float* part_sq;
+    int64_t foff[4], qoff[4], Fall, Fsq;
+    float* syy[2];
 };
+
+// One batch of all four matrices (bf16 caches, head_dim 128) in one launch:
+// kept rows stripped (keys), shifted, written feature-major as bf16 (hi, lo);
+// per-chunk column sums into part, per-chunk target sums of squares into part_sq.
+struct GatherAllArgs {
+    const __nv_bfloat16* cache[4];  // [n_slabs][T][128]
+    int64_t n_slabs[4];
+    int64_t foff[4];                // columns of matrix m in a row of part
+    int64_t qoff[4];                // columns of matrix m in a row of part_sq, -1 for sources
+    const float2* tab[4];           // RoPE table (keys) or NULL (values)
+    const float* mean_a[4];         // running means before the batch
+    float* shift[4];                // shift used, written
+    __nv_bfloat16* out[4];          // [n_slabs*128][ld]
+    __nv_bfloat16* out_lo[4];
+    int64_t T, ld, Fall, Fsq;
+    const int* rows;                // kept rows, [nb]
+    const int* nb;
+    const long long* n_seen;
+    const int* pos;
+    float* part;                    // [chunks][Fall]
+    float* part_sq;                 // [chunks][Fsq]
+    DevErr err;
+    int stride;                     // kept positions are multiples of it
+    int max_pos;                    // rows of the RoPE tables
+};
+bool gather_all_supported(kvb_dtype dt, int d);
+// tab_src / tab_tgt: the two RoPE tables (keys of matrices 0 and 2).
+cudaError_t launch_gather_all(const GatherAllArgs& a, int num_sms, cudaStream_t s);
 
 // One matrix of one batch: kept rows of `cache` [n_slabs][T][d] -> centered,
 // transposed operand out ([n_slabs*d][ld]; float32, or bf16 hi/lo if out_lo).
@@ -45,6 +80,23 @@ struct GatherArgs {
     int64_t ld;
 };
 bool gather_single_pass_ok(kvb_dtype dt, int d);
+
+// First batch only (device count *n_seen == 0): mean[m] = the column means of
+// the batch's first 128 kept rows (keys stripped), the shift of the
+// single-pass gathers.
+struct FirstMeanArgs {
+    const __nv_bfloat16* cache[4];
+    int64_t n_slabs[4];
+    const float2* tab[4];
+    float* mean[4];
+    int64_t T;
+    int d;
+    const int* rows;
+    const int* nb;
+    const long long* n_seen;
+    const int* pos;
+};
+cudaError_t launch_first_mean(const FirstMeanArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& g, cudaStream_t s);
 
 cudaError_t launch_select_rows(const int* pos, int64_t T, int stride, int max_pos, int* rows, int* nb, DevErr err,

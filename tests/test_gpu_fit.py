@@ -237,10 +237,12 @@ def test_persistent_and_per_tile_solver_updates_agree(kvb, monkeypatch):
     _check_fit(kvb, ctx, st, pair, torch.float32, TOL_W)
 
 
-@pytest.mark.parametrize("d,H", [(32, 8), (64, 4), (16, 16)])
+@pytest.mark.parametrize("d,H", [(32, 8), (64, 4), (16, 16), (128, 2)])
 def test_bf16_tensor_core_statistics_head_dims_packed_short_sequences(kvb, d, H):
     # H*d = 256, so the statistics run on the tensor cores; the single-pass gather
-    # uses its streaming kernel for head_dim 64 and the register kernel for 16 / 32.
+    # uses the four-matrix kernel for head_dim 128 (kept rows unevenly spaced at every
+    # sequence boundary: one copy per row), its streaming kernel for 64 and the
+    # register kernel for 16 / 32.
     # Each batch packs 200 sequences of 1-3 tokens (positions restart at 0), so
     # more rows are kept than T / stride and a CTA walks more than one chunk.
     rng = np.random.default_rng(d)
@@ -382,3 +384,56 @@ def test_reset_then_accumulate_again(kvb):
     assert kvb.kvb_stats_count(st) == 0
     _accumulate(kvb, ctx, st, pair["calib"], torch.bfloat16)
     _check_stats(kvb, st, pair, 1e-4)
+
+
+def test_four_matrix_gather_matches_oracle_and_per_matrix_path(kvb, monkeypatch):
+    # bf16 caches, head_dim 128, 8 -> 8 layers x 8 KV heads (8192 source and target features):
+    # the four matrices of a batch go through one gather launch (2048 items, ~13 per SM, so
+    # CTAs cross chunk and matrix boundaries), S_yy is updated in the merge.  Two batches:
+    # 4096 tokens (1024 kept rows, 8 chunks), then 3000 tokens at positions 7..3006 (750 kept
+    # rows, a ragged last chunk).  Checked against the oracle and against one launch per
+    # matrix (KVB_GATHER_ALL=0, which also keeps the separate S_yy pass and rounds the
+    # stripped keys once more): both within 1e-6 of each other.
+    import synth
+    L, H, d = 8, 8, 128
+    Fs = Ft = L * H * d
+    batches = []
+    for b, (T, p0) in enumerate(((4096, 0), (3000, 7))):
+        caches = [synth.torch_content(900 + 10 * b + i, L, H, T, d, 1.0, torch.bfloat16, "cuda") for i in range(4)]
+        batches.append((caches, torch.arange(p0, p0 + T, dtype=torch.int32, device="cuda")))
+    ctx = kvb.kvb_ctx_create(spec(L, H, d, 1e4), spec(L, H, d, 1e6), 2, 4096)
+    kvb.kvb_profile_enable(ctx, True)
+    st_all = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, 4096)
+    monkeypatch.setenv("KVB_GATHER_ALL", "0")
+    st_one = kvb.kvb_stats_create(ctx, kvb.KVB_BF16, 4096)
+    monkeypatch.delenv("KVB_GATHER_ALL")
+    for st in (st_all, st_one):
+        for caches, pos in batches:
+            kvb.kvb_stats_accumulate(ctx, st, *caches, pos, 4)
+    kvb.kvb_ctx_check(ctx)
+    kvb.kvb_profile_read(ctx)
+    # oracle: two-pass centered statistics over the kept rows of both batches
+    X, Y = {0: [], 1: []}, {0: [], 1: []}
+    for caches, pos in batches:
+        ph = pos.cpu().numpy()
+        keep = O.retain_stride(ph, 4)
+        sk, sv, tk, tv = (to_host64(c) for c in caches)
+        X[0].append(O.all_layer_features(sk, ph, 1e4)[keep])
+        X[1].append(O.all_layer_features(sv)[keep])
+        Y[0].append(O.all_layer_features(tk, ph, 1e6)[keep])
+        Y[1].append(O.all_layer_features(tv)[keep])
+    for kv in (0, 1):
+        ref = O.centered_stats(np.concatenate(X[kv]), np.concatenate(Y[kv]))
+        a = _export(kvb, st_all, kv, Fs, Ft)
+        b = _export(kvb, st_one, kv, Fs, Ft)
+        assert a[0] == b[0] == ref.n == 1024 + 750
+        # independent sources and targets: the cross statistics are sqrt(n)-sized noise, so
+        # their errors are also taken against the Cauchy-Schwarz scale sqrt(M_ii S_yy_j)
+        for got, want in zip(a[1:], (ref.xbar, ref.ybar, ref.M, ref.C, ref.syy)):
+            assert rel_fro(got, want) < 1e-4, rel_fro(got, want)
+        # per entry: fp32 accumulation in the tensor cores over ~110 K steps per batch
+        dm = np.sqrt(np.diag(ref.M))
+        assert np.max(np.abs(a[3] - ref.M) / np.outer(dm, dm)) < 5e-5
+        assert np.max(np.abs(a[4] - ref.C) / np.outer(dm, np.sqrt(ref.syy))) < 5e-5
+        for x, y in zip(a[1:], b[1:]):
+            assert rel_fro(x, y) <= 1e-6, rel_fro(x, y)

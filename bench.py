@@ -637,6 +637,49 @@ def attn_roofline(attn, clk):
 
 # --------------------------------------------------------------------------- GPU arm
 
+def run_library_reference(src, W, sel, steps, stream, dev, n_x=4):
+    """The map's own GEMMs on cuBLAS, as a like-for-like roofline reference.
+
+    One map is 2 x L_tgt GEMMs [T x k*H*d] . [k*H*d x H*d].  Here each is a
+    plain torch.matmul (cuBLAS bf16, fp32 accumulation) of a materialised
+    feature matrix X_t (the selected layers' rows of the same synthetic cache,
+    concatenated layer-major as the map reads them) and W_t, cycling over n_x
+    materialised targets, back to back for as many map-equivalents as the
+    timed region ran, on the launch stream.  No gather, strip, bias, RoPE or
+    target-layout store is done: it is the library doing only the contraction,
+    on the same data, shapes and duration as the map kernel.
+    """
+    import torch
+    L, H, T, d = src.shape
+    L_t = W.shape[0]
+    X = [torch.cat([src[int(s)].permute(1, 0, 2).reshape(T, H * d) for s in sel[t]], dim=1).contiguous()
+         for t in range(n_x)]
+    out = torch.empty((T, W.shape[1]), dtype=src.dtype, device=dev)
+
+    def one_map():
+        for i in range(2 * L_t):
+            torch.matmul(X[i % n_x], W[i % n_x].t(), out=out)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one_map()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one_map()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    flop = 2 * 2 * L_t * X[0].shape[1] * W.shape[1] * T
+    del X, out
+    return {"what": ("cuBLAS bf16 GEMM (torch.matmul) on the map's own 2 x L_tgt GEMMs per map, feature matrices "
+                     f"materialised from the same synthetic cache ({n_x} targets cycled) and the same W, back to "
+                     "back for as many maps as the timed region; no gather, strip, bias, RoPE or target-layout "
+                     "store"),
+            "ms_per_map_equiv": ms, "tflops": flop / (ms / 1e3) / 1e12, "maps": steps}
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import synth
@@ -716,6 +759,11 @@ def run_gpu(args, rank, world, local_rank):
             strip_alone = kvb.kvb_profile_read(ctx).get(STRIP_KERNEL)
         finally:
             del os.environ["KVB_MAP_FUSED_STRIP"]
+
+    library = None
+    if not args.skip_library and not args.skip_extras:
+        library = run_library_reference(src_v, W_v, sel_v, args.steps, stream, dev)
+        torch.cuda.empty_cache()
 
     if args.skip_extras:
         if rank == 0:
@@ -888,6 +936,8 @@ def run_gpu(args, rank, world, local_rank):
                                        if nominal else None),
                      "algorithmic_flop_per_launch": flop, "avg_launch_ms": gemm_avg,
                      "traffic": kernel_traffic(GEMM_KERNEL)},
+        "library_reference": (dict(library, map_kernel_speedup=library["ms_per_map_equiv"] / gemm_avg)
+                              if library else None),
         "hbm_pass": {"kernel": STRIP_KERNEL, "bound": "hbm", "achieved": strip_gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": (strip_gbs / peaks["hbm_gbs"]) if strip_gbs else None,
                      "algorithmic_bytes_per_launch": strip_bytes, "avg_launch_ms": strip_avg,
@@ -926,6 +976,8 @@ def main():
                     help="small: T=4096 with the same layer shapes (for profiler captures)")
     ap.add_argument("--skip-extras", action="store_true", help="skip the end-to-end, fit and CPU-baseline legs")
     ap.add_argument("--skip-fit", action="store_true", help="skip the calibration-statistics / fit leg")
+    ap.add_argument("--skip-library", action="store_true",
+                    help="skip the cuBLAS reference on the map's own GEMMs (same data, shapes and duration)")
     ap.add_argument("--skip-attn", action="store_true", help="skip the attention-output cosine leg")
     ap.add_argument("--attn-only", action="store_true", help="run only the attention-output cosine leg")
     ap.add_argument("--skip-fp32", action="store_true", help="skip the fp32-cache map leg")

@@ -201,33 +201,6 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
     }
 }
 
-// Stripped (keys) or raw (values) dims [8l, 8l+8) and [half+8l, half+8l+8) of one row.
-__device__ __forceinline__ void pair8(const __nv_bfloat16* __restrict__ row, int l, int half, bool strip,
-                                      const float2* __restrict__ tab_row, float (&lo)[8], float (&hi)[8]) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(row + 8 * l));
-    const uint4 b = __ldg(reinterpret_cast<const uint4*>(row + half + 8 * l));
-    float x[8], y[8];
-    unpack8(a, x);
-    unpack8(b, y);
-    if (!strip) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            lo[i] = x[i];
-            hi[i] = y[i];
-        }
-        return;
-    }
-    const float4* t4 = reinterpret_cast<const float4*>(tab_row + 8 * l);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float4 cs = __ldg(t4 + q);  // (c, s) of pairs 2q and 2q+1
-        lo[2 * q] = fmaf(x[2 * q], cs.x, y[2 * q] * cs.y);
-        hi[2 * q] = fmaf(y[2 * q], cs.x, -(x[2 * q] * cs.y));
-        lo[2 * q + 1] = fmaf(x[2 * q + 1], cs.z, y[2 * q + 1] * cs.w);
-        hi[2 * q + 1] = fmaf(y[2 * q + 1], cs.z, -(x[2 * q + 1] * cs.w));
-    }
-}
-
 constexpr int kChunk = 128;  // kept rows per CTA of the single-pass gather
 
 // Grid (chunk group, slab), 256 threads; a CTA takes chunks blockIdx.x,

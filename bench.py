@@ -509,6 +509,9 @@ def run_map_pair(kvb, dev, name, seed=211):
     kern = kvb.kvb_profile_read(ctx)
     g_n, g_ms = kern.get(GEMM_KERNEL, (0, 0.0))
     g_avg = g_ms / max(g_n, 1)
+    del out_k, out_v
+    library = run_library_reference(src_v, W_v, sel_v, reps, stream, dev, n_x=2)
+    library["map_kernel_speedup"] = library["ms_per_map_equiv"] / g_avg if g_avg > 0 else None
     flop = 2 * 2 * L_t * p * q * T
     achieved = flop / (g_avg / 1e3) / 1e12 if g_ms else None
     peaks, peak_kind = measured_peaks()
@@ -522,7 +525,7 @@ def run_map_pair(kvb, dev, name, seed=211):
     Wk_h = np.transpose(hs(W_k.index_select(0, li)), (0, 2, 1))
     Wv_h = np.transpose(hs(W_v.index_select(0, li)), (0, 2, 1))
     bk_h, bv_h = hs(b_k.index_select(0, li)), hs(b_v.index_select(0, li))
-    del src_k, src_v, W_k, W_v, out_k, out_v
+    del src_k, src_v, W_k, W_v
     kvb.kvb_ctx_destroy(ctx)
     torch.cuda.empty_cache()
     t0 = time.perf_counter()
@@ -537,6 +540,7 @@ def run_map_pair(kvb, dev, name, seed=211):
                          "frac": achieved / peaks["bf16_tflops"] if achieved else None,
                          "peak_kind": f"{peak_kind} bf16 burst (each launch runs alone)",
                          "algorithmic_flop_per_launch": flop, "avg_launch_ms": g_avg},
+            "library_reference": library,
             "cpu_baseline": {"value": cpu_rate, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
                              "sample": f"{n_l} of {L_t} target layers x {T_cpu} tokens, float64, scaled to a full map",
                              "seconds": cpu_s}}

@@ -91,10 +91,6 @@ struct __align__(16) SumDest {
     int64_t sum_off, sq_off;
 };
 
-__device__ __forceinline__ float2 bf2(uint32_t w) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-}
-
 // Tensor maps of the four caches ([slabs][T][128] bf16, box 128 x rows*stride x 1,
 // element strides 1 x stride x 1) and of the two RoPE tables ([max_pos][128]
 // fp32, box 128 x rows*stride, element strides 1 x stride).  rows = 0: none.

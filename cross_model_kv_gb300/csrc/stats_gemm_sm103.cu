@@ -8,8 +8,8 @@
 // g za zb the rank-1 term that centers it on the batch mean and f da db the
 // rank-1 Chan term between the running and the batch means.  The operands are bf16 pairs
 // (hi + lo) of the float32 centered values; the product is accumulated as
-// hi.hi + hi.lo + lo.hi in one fp32 TMEM accumulator, three K-passes over the
-// same tile, which keeps ~16 significant bits per operand.
+// lo.hi + hi.lo + hi.hi (smallest first) in one fp32 TMEM accumulator, three
+// K-passes over the same tile, which keeps ~16 significant bits per operand.
 //
 // Persistent, warp-specialised, 128 x 256 tiles on one CTA per SM, or 256 x
 // 256 tiles on CTA pairs (stats_gemm_pair_kernel, the default when the sizes
@@ -86,10 +86,14 @@ struct Maps {
     CUtensorMap a[3][4], b[3][4];  // [part: hi, lo, third][job]
 };
 
-// Operand parts of product `seg`, largest first: two-part operands take
+// Operand parts of product `seg` in order of size: two-part operands take
 // hi.hi, hi.lo, lo.hi; three-part operands add hi.3, lo.lo, 3.hi (every product
 // down to 2^-16 of the leading one).  The part indices are packed four bits per
-// product so that the single producer thread computes them in registers.
+// product so that the single producer thread computes them in registers.  The
+// products are issued smallest first (product nprod - 1 down to 0): the small
+// ones then add into a small accumulator instead of losing their low bits
+// against the full-size sum, which leaves the statistics (and W on
+// ill-conditioned systems) measurably closer to float64 at the same cost.
 __device__ __forceinline__ void product_maps(const Maps& M, int job, int seg, const CUtensorMap*& ma,
                                              const CUtensorMap*& mb) {
     constexpr uint32_t PA = 0x210100u, PB = 0x012010u;  // parts of A and B for products 0..5
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 int job, bi, bj;
                 decode(P.tiles[t], job, bi, bj);
                 const CUtensorMap *ma, *mb;
-                product_maps(M, job, 0, ma, mb);
+                product_maps(M, job, P.nprod - 1, ma, mb);
                 for (int it = 0, seg = 0, kb = 0; it < iters; ++it) {  // it = seg * nk + kb
                     if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) {
                         ok = false;
@@ -221,7 +225,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tma_load_2d(sB + stage * B_BYTES, mb, &full[stage], kb * BK, bj * BN);
                     if (++kb == nk && ++seg < P.nprod) {
                         kb = 0;
-                        product_maps(M, job, seg, ma, mb);
+                        product_maps(M, job, P.nprod - 1 - seg, ma, mb);
                     }
                     issued_phase[stage] = static_cast<int>(phase);
                     if (++stage == STAGES) {
@@ -419,7 +423,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 int job, bi, bj;
                 decode(P.tiles[t], job, bi, bj);
                 const CUtensorMap *ma, *mb;
-                product_maps(M, job, 0, ma, mb);
+                product_maps(M, job, P.nprod - 1, ma, mb);
                 for (int it = 0, seg = 0, kb = 0; it < iters; ++it) {  // it = seg * nk + kb
                     if (!mbar_wait(&empty[stage], phase ^ 1u, P.err, abort_flag)) {
                         ok = false;
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tma_load_2d_pair(sB + stage * PA_BYTES, mb, full_leader, kb * BK, bj * PM + 128 * rank);
                     if (++kb == nk && ++seg < P.nprod) {
                         kb = 0;
-                        product_maps(M, job, seg, ma, mb);
+                        product_maps(M, job, P.nprod - 1 - seg, ma, mb);
                     }
                     issued_phase[stage] = static_cast<int>(phase);
                     if (++stage == PSTAGES) {

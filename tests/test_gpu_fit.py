@@ -351,6 +351,34 @@ def test_no_observations_and_zero_lambda_is_a_numeric_error(kvb):
     assert e.value.status == 5
 
 
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 16)])
+def test_non_finite_calibration_value_is_a_numeric_error(kvb, dtype, d):
+    # One NaN in one source value reaches the statistics of its feature; the
+    # factorisations meet a pivot that is not a positive number and the fit calls
+    # return KVB_ERR_NUMERIC instead of a selection or W built on it.
+    pair = make_pair(22, 3, 2, 2, d, 2, 256, 4, 1e4, 1e6, noise=1e-2, sigma=1.0)
+    if dtype == torch.bfloat16:
+        pair = round_pair(pair, torch.bfloat16)
+    src_k, src_v, tgt_k, tgt_v, pos = pair["calib"][1]
+    src_v = src_v.copy()
+    src_v[1, 0, 40, 3] = np.nan
+    pair["calib"][1] = (src_k, src_v, tgt_k, tgt_v, pos)
+    ctx = _ctx(kvb, pair, 256)
+    st = kvb.kvb_stats_create(ctx, kvb.KVB_BF16 if dtype == torch.bfloat16 else kvb.KVB_F32, 256)
+    _accumulate(kvb, ctx, st, pair["calib"], dtype)
+    with pytest.raises(kvb.KvbError) as e:
+        kvb.kvb_layer_select(ctx, st, 0.01)
+    assert e.value.status == 5
+    q = pair["H"] * d
+    Wk = torch.empty((2, q, 2 * q), dtype=torch.float32, device="cuda")
+    bk = torch.empty((2, q), dtype=torch.float32, device="cuda")
+    sel = np.array([[0, 1], [1, 2]], dtype=np.int32)  # both systems of V read source layer 1
+    with pytest.raises(kvb.KvbError) as e:
+        kvb.kvb_ridge_solve(ctx, st, sel, sel, 0.01, Wk, Wk.clone(), bk, bk.clone())
+    assert e.value.status == 5
+    kvb.kvb_ctx_check(ctx)  # the context itself stays usable
+
+
 def test_top_k_equal_to_all_source_layers(kvb):
     # k = L_src: every source layer is selected; the fit uses all of them.
     pair = make_pair(22, 3, 2, 2, 16, 3, 256, 4, 1e4, 5e4)

@@ -13,7 +13,10 @@ import os
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_lib", "libkvb.so")
+# KVB_LIBRARY=checked loads the checked build (index checks on the hot kernels'
+# CUDA-core global accesses; build.build(checked=True) makes it)
+LIB_PATH = os.path.join(_HERE, "_lib", "libkvb_checked.so" if os.environ.get("KVB_LIBRARY") == "checked"
+                        else "libkvb.so")
 
 KVB_OK = 0
 KVB_ERR_INVALID_ARG = 1

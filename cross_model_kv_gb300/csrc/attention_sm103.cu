@@ -430,7 +430,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     nb += xch[256 + row];
                     const float den = sqrtf(na) * sqrtf(nb);
                     const int hq = kh * g + grow / P.Tq;
-                    P.cos_out[(static_cast<int64_t>(l) * P.Hq + hq) * P.Tq + grow % P.Tq] = den > 0.f ? dot / den : 0.f;
+                    const int64_t oi = (static_cast<int64_t>(l) * P.Hq + hq) * P.Tq + grow % P.Tq;
+                    if (KVB_IN_BOUNDS(P.err, oi, 1, static_cast<int64_t>(P.L) * P.Hq * P.Tq))
+                        P.cos_out[oi] = den > 0.f ? dot / den : 0.f;
                 }
             }
         }

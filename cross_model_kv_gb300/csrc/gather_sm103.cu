@@ -328,7 +328,8 @@ __global__ void __launch_bounds__(GTHREADS, 1) gather_all_kernel(const __grid_co
         const float* shift = reinterpret_cast<const float*>(sm + G_OFF_SHIFT + s * G_SHIFT);
         const float shl = shift[i], shh = shift[GHALF + i];
         const int64_t f0 = cur.slab * GD;
-        if (cur.chunk == 0 && q == 0) {
+        const int64_t F_m = A.n_slabs[m] * GD;  // features of this matrix
+        if (cur.chunk == 0 && q == 0 && KVB_IN_BOUNDS(err, f0 + i, GHALF + 1, F_m)) {
             p_shift[f0 + i] = shl;
             p_shift[f0 + GHALF + i] = shh;
         }
@@ -369,6 +370,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) gather_all_kernel(const __grid_co
 #pragma unroll
         for (int f = 0; f < 2; ++f) {
             const int64_t o = (f0 + f * GHALF + i) * A.ld + r0 + q * GRPW;
+            if (!KVB_IN_BOUNDS(err, o, GRPW, F_m * A.ld)) continue;
             uint32_t hw[8], lw[8];
 #pragma unroll
             for (int w = 0; w < 8; ++w) {

@@ -74,6 +74,8 @@ kvb_status take_device_error(kvb_ctx* c) {
     cudaMemset(c->err_dev, 0, sizeof(int));
     if (code == DEV_ERR_TIMEOUT)
         return fail(KVB_ERR_TIMEOUT, "a bounded device wait gave up in an earlier kernel on this context");
+    if (code == DEV_ERR_BOUNDS)
+        return fail(KVB_ERR_CUDA, "an index check of the checked build failed in an earlier kernel on this context");
     return fail(KVB_ERR_INVALID_ARG, "a position outside [0, max_pos) was seen by an earlier kernel on this context");
 }
 

@@ -117,6 +117,8 @@ __device__ __forceinline__ void strip_chunk(const Params& P, int item, int lane)
         const int tok = t0 + r;
         if (tok >= P.T) break;
         const int64_t o = (static_cast<int64_t>(slab) * P.T + tok) * P.d + c8;
+        const int64_t strip_size = static_cast<int64_t>(P.strip_items / P.strip_chunks) * P.T * P.d;
+        if (!KVB_IN_BOUNDS(P.err, o, 8, strip_size) || !KVB_IN_BOUNDS(P.err, o + half, 8, strip_size)) continue;
         const int p = __ldg(P.pos + tok);
         uint4 olo = make_uint4(0, 0, 0, 0), ohi = make_uint4(0, 0, 0, 0);
         if (p < 0 || p >= P.max_pos) {
@@ -234,6 +236,14 @@ __device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c
         for (int hh = 0; hh < heads_per_tile; ++hh) {
             const int h = c.n * heads_per_tile + hh;
             const int64_t orow = ((static_cast<int64_t>(c.t) * P.H + h) * P.T + tok) * P.d;
+            // checked build: the bias reads and the row's stores stay inside their
+            // buffers (the TMEM loads below are warp-wide and always run)
+            const int64_t out_size = static_cast<int64_t>(P.L_t) * P.H * P.T * P.d;
+            const int64_t boff = static_cast<int64_t>(c.t) * q + c.n * BN + hh * P.d + e0;
+            const bool inb = KVB_IN_BOUNDS(P.err, boff, 16, static_cast<int64_t>(P.L_t) * q) &&
+                             KVB_IN_BOUNDS(P.err, boff + half, 16, static_cast<int64_t>(P.L_t) * q) &&
+                             (!valid || (KVB_IN_BOUNDS(P.err, orow + e0, 16, out_size) &&
+                                         KVB_IN_BOUNDS(P.err, orow + half + e0, 16, out_size)));
             uint32_t lo[16], hi[16];
             tmem_ld16(tbase + hh * P.d + e0, lo);
             tmem_ld16(tbase + hh * P.d + half + e0, hi);
@@ -243,8 +253,8 @@ __device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c
             const float4* bh = reinterpret_cast<const float4*>(bias + hh * P.d + half + e0);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-                const float4 a = __ldg(bl + v);
-                const float4 b = __ldg(bh + v);
+                const float4 a = inb ? __ldg(bl + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 b = inb ? __ldg(bh + v) : make_float4(0.f, 0.f, 0.f, 0.f);
                 xl[4 * v + 0] = __uint_as_float(lo[4 * v + 0]) + a.x;
                 xl[4 * v + 1] = __uint_as_float(lo[4 * v + 1]) + a.y;
                 xl[4 * v + 2] = __uint_as_float(lo[4 * v + 2]) + a.z;
@@ -265,7 +275,7 @@ __device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c
                     xh[2 * v + 1] = fmaf(h1, cs[v].z, l1 * cs[v].w);
                 }
             }
-            if (valid && F32OUT) {
+            if (valid && inb && F32OUT) {
                 float* o = static_cast<float*>(P.out[c.kv]) + orow;
 #pragma unroll
                 for (int v = 0; v < 2; ++v) {  // 8 outputs = one 32-byte sector per store
@@ -278,7 +288,7 @@ __device__ __forceinline__ void epilogue_row(const Params& P, const TileCoord& c
                     st_global_v8(o + e0 + 8 * v, a);
                     st_global_v8(o + half + e0 + 8 * v, b);
                 }
-            } else if (valid) {
+            } else if (valid && inb) {
                 __nv_bfloat16* o = static_cast<__nv_bfloat16*>(P.out[c.kv]) + orow;
                 uint32_t pl[8], ph[8];
 #pragma unroll

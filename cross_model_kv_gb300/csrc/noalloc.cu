@@ -193,6 +193,7 @@ extern "C" kvb_status kvb_map_apply_noalloc(const kvb_model_spec* src, const kvb
     if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
     if (e != cudaSuccess) return cuda_fail(e, "kvb_map_apply_noalloc");
     if (code == DEV_ERR_TIMEOUT) return fail(KVB_ERR_TIMEOUT, "kvb_map_apply_noalloc: a bounded device wait gave up");
+    if (code == DEV_ERR_BOUNDS) return fail(KVB_ERR_CUDA, "kvb_map_apply_noalloc: an index check of the checked build failed");
     if (code != 0)
         return fail(KVB_ERR_INVALID_ARG, "kvb_map_apply_noalloc: a position outside [0, max_pos) (row written as zeros)");
     return KVB_OK;

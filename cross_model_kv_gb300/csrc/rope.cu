@@ -50,6 +50,9 @@ __global__ void __launch_bounds__(256) strip_bf16_vec_kernel(const __nv_bfloat16
         const int e0 = c * 8;
         const __nv_bfloat16* src = in + row * d + e0;
         __nv_bfloat16* dst = out + row * d + e0;
+        if (!KVB_IN_BOUNDS(err, row * d + e0, 8, rows * d) || !KVB_IN_BOUNDS(err, row * d + e0 + half, 8, rows * d) ||
+            !KVB_IN_BOUNDS(err, tok, 1, T))
+            continue;
         const int p = __ldg(pos + tok);
         if (p < 0 || p >= max_pos) {
             dev_err_set(err, DEV_ERR_BAD_POS);
@@ -58,6 +61,7 @@ __global__ void __launch_bounds__(256) strip_bf16_vec_kernel(const __nv_bfloat16
             *reinterpret_cast<uint4*>(dst + half) = z;
             continue;
         }
+        if (!KVB_IN_BOUNDS(err, static_cast<int64_t>(p) * half + e0, 8, static_cast<int64_t>(max_pos) * half)) continue;
         const uint4 vlo = __ldcs(reinterpret_cast<const uint4*>(src));
         const uint4 vhi = __ldcs(reinterpret_cast<const uint4*>(src + half));
         const float4* tp = reinterpret_cast<const float4*>(tab + static_cast<int64_t>(p) * half + e0);

@@ -82,11 +82,28 @@ struct DevErr {
     uint64_t timeout_ns;  // limit of every spin-wait
 };
 
-enum : int { DEV_ERR_NONE = 0, DEV_ERR_BAD_POS = 1, DEV_ERR_TIMEOUT = 7 };
+enum : int { DEV_ERR_NONE = 0, DEV_ERR_BAD_POS = 1, DEV_ERR_TIMEOUT = 7, DEV_ERR_BOUNDS = 9 };
 
 __device__ __forceinline__ void dev_err_set(const DevErr& e, int code) {
     if (e.word) atomicCAS(e.word, 0, code);
 }
+
+// Index checks of the checked build (-DKVB_CHECK_BOUNDS=1, libkvb_checked.so),
+// standing in for a memory checker: the CUDA-core global accesses of the hot
+// kernels ask KVB_IN_BOUNDS(err, first element, elements, buffer size) before
+// touching memory; a failing check records DEV_ERR_BOUNDS and the access is
+// skipped.  In the normal build the macro is the constant true.
+__device__ __forceinline__ bool check_bounds(const DevErr& e, int64_t first, int64_t count, int64_t size) {
+    if (first >= 0 && count >= 0 && first + count <= size) return true;
+    dev_err_set(e, DEV_ERR_BOUNDS);
+    return false;
+}
+#if defined(KVB_CHECK_BOUNDS) && KVB_CHECK_BOUNDS
+#define KVB_IN_BOUNDS(err, first, count, size) ::kvb::check_bounds((err), (first), (count), (size))
+#else  // the arguments are named (not evaluated) so that their variables count as used
+#define KVB_IN_BOUNDS(err, first, count, size) \
+    ((void)sizeof(err), (void)sizeof(first), (void)sizeof(count), (void)sizeof(size), true)
+#endif
 
 // Wait for `parity` on `bar`; gives up after e.timeout_ns (recording
 // DEV_ERR_TIMEOUT) or as soon as *abort is set by another role of the CTA.

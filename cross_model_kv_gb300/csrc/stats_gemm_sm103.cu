@@ -69,6 +69,7 @@ struct JobP {
     const float* za;
     const float* zb;
     int64_t ldo;
+    int64_t rows, cols;  // out is [rows][ldo]; da, za have rows entries, db, zb cols
 };
 
 struct Params {
@@ -114,16 +115,21 @@ __device__ __forceinline__ void decode(uint32_t e, int& job, int& bi, int& bj) {
 __device__ __forceinline__ void merge_row(const Params& P, int job, int64_t i, int64_t j0, uint32_t tbase,
                                           bool have_acc, float fda, float gza) {
     const JobP J = P.job[job];
+    // checked build: the row's statistics and merge vectors stay inside their buffers
+    // (the TMEM loads below are warp-wide and always run)
+    const bool inb = KVB_IN_BOUNDS(P.err, i * J.ldo + j0, 128, J.rows * J.ldo) && KVB_IN_BOUNDS(P.err, j0, 128, J.cols);
     float* orow = J.out + i * J.ldo + j0;
     const float* dbp = J.db + j0;
     const float* zbp = J.zb + j0;
-    uint32_t cur[2][8];
-    ld_global_v8(orow, cur[0]);
-    ld_global_v8(orow + 8, cur[1]);
+    uint32_t cur[2][8] = {};
+    if (inb) {
+        ld_global_v8(orow, cur[0]);
+        ld_global_v8(orow + 8, cur[1]);
+    }
 #pragma unroll 1
     for (int c0 = 0; c0 < 128; c0 += 16) {
-        uint32_t nxt[2][8];
-        if (c0 + 16 < 128) {
+        uint32_t nxt[2][8] = {};
+        if (inb && c0 + 16 < 128) {
             ld_global_v8(orow + c0 + 16, nxt[0]);
             ld_global_v8(orow + c0 + 24, nxt[1]);
         }
@@ -140,8 +146,10 @@ __device__ __forceinline__ void merge_row(const Params& P, int job, int64_t i, i
             uint32_t o[8];
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
-                const float4 d = __ldg(reinterpret_cast<const float4*>(dbp + c0 + 8 * h + 4 * v));
-                const float4 z = __ldg(reinterpret_cast<const float4*>(zbp + c0 + 8 * h + 4 * v));
+                const float4 d = inb ? __ldg(reinterpret_cast<const float4*>(dbp + c0 + 8 * h + 4 * v))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 z = inb ? __ldg(reinterpret_cast<const float4*>(zbp + c0 + 8 * h + 4 * v))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                 const float dd[4] = {d.x, d.y, d.z, d.w}, zz[4] = {z.x, z.y, z.z, z.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -150,7 +158,7 @@ __device__ __forceinline__ void merge_row(const Params& P, int job, int64_t i, i
                                            fda * dd[u] - gza * zz[u]);
                 }
             }
-            st_global_v8(orow + c0 + 8 * h, o);
+            if (inb) st_global_v8(orow + c0 + 8 * h, o);
         }
         if (c0 + 16 < 128) {
 #pragma unroll
@@ -627,7 +635,7 @@ cudaError_t launch_stats_gemm_tc(StatsGemmPlan* plan, const StatsJob* jobs, int 
             !encode_2d(&M.b[0][j], J.B, ld, J.Nb, pair ? 128 : BN, why) ||
             !encode_2d(&M.b[1][j], J.B_lo, ld, J.Nb, pair ? 128 : BN, why))
             return cudaErrorInvalidValue;
-        P.job[j] = JobP{J.out, J.da, J.db, J.za, J.zb, J.ldo};
+        P.job[j] = JobP{J.out, J.da, J.db, J.za, J.zb, J.ldo, J.Ma, J.Nb};
     }
     if (pair) {
         cudaError_t e = cudaMemsetAsync(plan->ctr, 0, sizeof(int), s);

@@ -57,6 +57,11 @@
  * fixed tile-per-pair map, separate strip pass, single-CTA statistics,
  * per-tile solver updates, CUDA-core statistics for fp32 caches); results
  * agree with the defaults within rounding.
+ *
+ * Checked build: the same library compiled with KVB_CHECK_BOUNDS=1
+ * (libkvb_checked.so) checks the index range of every CUDA-core global access
+ * of the hot kernels before it happens; a failed check skips the access and
+ * the next call on the context returns KVB_ERR_CUDA.
  */
 #ifndef KVB_H
 #define KVB_H

@@ -94,7 +94,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     if _lib is not None:
         return _lib
     if not os.path.exists(path):
-        raise RuntimeError(f"libkvb.so is not built ({path}); run cross_model_kv_gb300.build.build()")
+        how = "build(checked=True)" if path.endswith("_checked.so") else "build()"
+        raise RuntimeError(f"{os.path.basename(path)} is not built ({path}); run cross_model_kv_gb300.build.{how}")
     lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         f = getattr(lib, name)
